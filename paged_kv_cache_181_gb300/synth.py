@@ -1,0 +1,84 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
+
+This module holds random draws only -- no arithmetic of the method.  One
+``torch.Generator`` per (workload, layer) draws, in this order:
+
+1. the pool permutation (block allocation): every row gets ``ceil(end / bs)``
+   logical blocks for its video positions, then ``ceil(action_len / bs)``
+   scratch blocks for its action tokens, taken in turn from a random
+   permutation of blocks ``1 .. pool_blocks-1``.  Block 0 is never handed out:
+   it is the table's padding entry, so a test can poison it;
+2. Q ``[B * q_len, Hq, D]`` ~ N(0, sigma);
+3. history K, V ``[B, history, Hkv, D]`` ~ N(0, sigma);
+4. current K, V ``[B * q_len, Hkv, D]`` ~ N(0, sigma) (video tokens, then the
+   row's action tokens).
+
+Values are drawn in float32 and rounded to the workload dtype
+(round-to-nearest-even), so the oracle can upcast the exact same numbers.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from .configs import Workload
+
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@dataclass
+class Draw:
+    workload: Workload
+    layer: int
+    row_blocks: list        # per row: int64 tensor, physical block of each logical video block
+    action_blocks: list     # per row: int64 tensor, scratch blocks for action tokens
+    q: torch.Tensor         # [B*q_len, Hq, D]
+    k_hist: torch.Tensor    # [B, history, Hkv, D]
+    v_hist: torch.Tensor
+    k_cur: torch.Tensor     # [B*q_len, Hkv, D]
+    v_cur: torch.Tensor
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def seed_of(w: Workload, layer: int) -> int:
+    return w.seed * 1000 + layer
+
+
+def draw(w: Workload, layer: int = 0, device="cpu") -> Draw:
+    """Draw one layer's inputs for workload ``w`` on ``device``."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed_of(w, layer))
+    dt = TORCH_DTYPE[w.dtype]
+    bs = w.block_size
+    n_video = _ceil_div(w.end_tokens, bs)
+    n_action = _ceil_div(w.action_len, bs)
+    per_row = n_video + n_action
+    if w.batch * per_row > w.pool_blocks - 1:
+        raise ValueError(f"{w.name}: pool of {w.pool_blocks} blocks cannot hold {w.batch} rows of {per_row}")
+    perm = torch.randperm(w.pool_blocks - 1, generator=g, device=dev) + 1
+    perm = perm.to("cpu", torch.int64)
+    row_blocks, action_blocks = [], []
+    for b in range(w.batch):
+        base = b * per_row
+        row_blocks.append(perm[base : base + n_video].clone())
+        action_blocks.append(perm[base + n_video : base + per_row].clone())
+
+    def normal(*shape):
+        x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+        if w.sigma != 1.0:
+            x.mul_(w.sigma)
+        return x.to(dt)
+
+    tq = w.batch * w.q_len
+    q = normal(tq, w.num_heads, w.head_dim)
+    k_hist = normal(w.batch, w.history_tokens, w.num_kv_heads, w.head_dim)
+    v_hist = normal(w.batch, w.history_tokens, w.num_kv_heads, w.head_dim)
+    k_cur = normal(tq, w.num_kv_heads, w.head_dim)
+    v_cur = normal(tq, w.num_kv_heads, w.head_dim)
+    return Draw(w, layer, row_blocks, action_blocks, q, k_hist, v_hist, k_cur, v_cur)
