@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark: one forward of chunk-wise paged self-attention per step.
+
+A step is the whole hot path for one forward of the long-window workload:
+for each of the 40 layers, the slot-mapping KV write of the current chunk
+into that layer's pools, then paged attention of the chunk's queries over the
+visible window (1 sink frame + 16 recent frames, 26520 keys) for both CFG
+branches.  The per-forward host metadata is built once (as the pages build it
+once per forward for all layers) and is not part of the device timing; the
+``e2e`` figure re-uploads it every step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  Timing: CUDA events on the launching stream,
+barrier + synchronize on both sides, max over ranks.  Inputs are larger than
+L2 (every layer has its own 1.1 GB of pools, so each layer's keys are cold).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged attention TFLOP/s (% bf16 peak); KV-write GB/s (% HBM peak)"
+DEFAULT_WORKLOAD = "long-window-40L-bf16"
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def visible_pairs(meta) -> int:
+    """Visible (query, key) pairs summed over rows, from the library's host metadata."""
+    pairs = 0
+    for b in range(len(meta.seq_lens)):
+        sq = int(meta.query_start_loc[b + 1] - meta.query_start_loc[b])
+        L = int(meta.seq_lens[b])
+        off = L - sq
+        segs = meta.segments[b] if meta.segments is not None and meta.segments[b] else [(off, L, L, 1)]
+        for (s, e, kv_end, mode) in segs:
+            n = e - s
+            kv_end = min(kv_end, L)
+            if mode == 1:
+                pairs += n * kv_end
+            else:
+                shift = kv_end - n
+                # rows r = 0..n-1 see min(kv_end, r + shift + 1) keys (clamped at 0)
+                for r in range(n):
+                    pairs += max(0, min(kv_end, r + shift + 1))
+    return pairs
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+
+def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int | None = None) -> dict:
+    """Time the float32 oracle on a bounded sample of the workload (layer 0, row 0, whole heads)."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import pagedattn as pa
+    from paged_kv_cache_181_gb300 import synth
+    from tests import cases
+
+    import dataclasses
+
+    w1 = dataclasses.replace(w, batch=1, layers=1)
+    d = synth.draw(w1, 0, "cpu")
+    oc = cases.oracle_metadata(w1)
+    cases.oracle_pools(w1, d, oc)
+    heads = list(range(w1.num_heads if max_heads is None else min(max_heads, w1.num_heads)))
+    flops = 0
+    done = 0
+    t0 = time.perf_counter()
+    for h in heads:
+        sample = {(0, h): np.arange(w1.q_len)}
+        pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, w1.head_dim ** -0.5,
+                           w1.block_size, oc.segments, dtype=np.float32, sample=sample)
+        flops += pa.attention_flops(oc.qsl, oc.seq_lens, oc.segments, 1, w1.head_dim)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) if threadpool_info() else os.cpu_count()
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{w.name}: layer 0, branch 0, {done} of {w.num_heads} heads x {w.q_len} queries x "
+                      f"{int(oc.seq_lens[0])} keys, float32 NumPy oracle ({dt:.1f} s)", "seconds": dt}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from paged_kv_cache_181_gb300 import configs
+
+    w = configs.ALL[args.workload]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, budget_s=1.0, max_heads=1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_oracle_sample(w, budget_s=8.0))
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "sample": vals[0]["sample"]},
+        "cpu_baseline": {k: vals[0][k] for k in ("unit", "cores", "kind", "sample")} | {"value": v},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU leg
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_181_gb300 import _lib, configs, workload
+
+    w = configs.ALL[args.workload]
+    peaks = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workload.build_case(w, device=dev, poison=False)
+    meta = case.meta
+    layers = case.layers
+    pairs = visible_pairs(meta)
+    flops_per_layer = 4 * w.head_dim * w.num_heads * pairs
+    tq = int(meta.query_start_loc[-1])
+    row_bytes = w.num_kv_heads * w.head_dim * (2 if w.dtype != "f32" else 4)
+    write_bytes_per_layer = tq * 2 * (2 * row_bytes) + tq * 8  # read + write of K and V rows, plus the slot ids
+    stream = torch.cuda.current_stream()
+
+    def step():
+        case.step(stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # Per-launch durations over separate instrumented steps (events between launches).
+    ev_w = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    write_ms, attn_ms, launch_log = [], [], []
+    for _ in range(max(1, min(args.steps, 3))):
+        for l in range(layers):
+            ev_w[l][0].record(stream)
+            case.write(l, stream=stream)
+            ev_w[l][1].record(stream)
+            ev_a[l][0].record(stream)
+            case.attend(l, stream=stream)
+            attn_launches_l = _lib.last_launches()
+            ev_a[l][1].record(stream)
+            launch_log.append(attn_launches_l)
+        torch.cuda.synchronize()
+        write_ms += [ev_w[l][0].elapsed_time(ev_w[l][1]) for l in range(layers)]
+        attn_launches = launch_log[-layers:]
+        attn_ms += [ev_a[l][0].elapsed_time(ev_a[l][1]) for l in range(layers)]
+
+    # Timed region: K whole steps.
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    ms_step = ms / args.steps
+    total_flops = flops_per_layer * layers * world
+    value = total_flops / (ms_step * 1e-3) / 1e12
+
+    attn_avg = statistics.mean(attn_ms)
+    write_avg = statistics.mean(write_ms)
+    attn_tflops = flops_per_layer / (attn_avg * 1e-3) / 1e12
+    write_gbs = write_bytes_per_layer / (write_avg * 1e-3) / 1e9
+    launches_per_step = sum(1 + attn_launches[l] for l in range(layers))
+
+    traffic = None
+    traffic_path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if os.path.exists(traffic_path):
+        try:
+            with open(traffic_path) as f:
+                t = json.load(f)
+            if t.get("workload") == w.name and t.get("kernel_rev") == KERNEL_REV:
+                traffic = t["bytes_per_launch"]
+        except Exception:
+            traffic = None
+
+    # e2e: inputs from pinned host memory every step, outputs back to the host.
+    e2e = run_e2e(case, args, world, stream) if not args.no_e2e else None
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1), shapes of 832x480 frames)",
+        "config": {"workload": w.name, "layers": layers, "batch": w.batch, "heads": w.num_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "q_len": w.q_len,
+                   "kv_len": int(meta.seq_lens[0]), "block_size": w.block_size, "pool_blocks_per_layer": w.pool_blocks,
+                   "l2": "inputs larger than L2: each layer reads its own %.2f GB of pools" %
+                         (2 * w.pool_blocks * 16 * row_bytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                     "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                     "kernel": "paged attention", "ms_per_launch": attn_avg,
+                     "algorithmic_flops_per_launch": flops_per_layer},
+        "kv_write": {"bound": "hbm", "achieved": write_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": write_gbs / peaks["hbm_gbs"], "ms_per_launch": write_avg,
+                     "algorithmic_bytes_per_launch": write_bytes_per_layer},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = {k: v for k, v in cpu_oracle_sample(w).items() if k != "seconds"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+KERNEL_REV = "simt-v0"
+
+
+def run_e2e(case, args, world, stream):
+    import torch
+
+    from paged_kv_cache_181_gb300 import _lib
+
+    layers = case.layers
+    host_q = [t.cpu().pin_memory() for t in case.q]
+    host_k = [t.cpu().pin_memory() for t in case.k_new]
+    host_v = [t.cpu().pin_memory() for t in case.v_new]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in case.out]
+    meta_host = [t.cpu().pin_memory() for t in (case.slots, case.block_table, case.query_start_loc, case.seq_lens)]
+    meta_dev = [case.slots, case.block_table, case.query_start_loc, case.seq_lens]
+    if case.segs is not None:
+        meta_host += [case.segs.cpu().pin_memory(), case.seg_start.cpu().pin_memory()]
+        meta_dev += [case.segs, case.seg_start]
+    h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v + meta_host)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for hd, dd in zip(meta_host, meta_dev):
+            dd.copy_(hd, non_blocking=True)
+        for l in range(layers):
+            case.q[l].copy_(host_q[l], non_blocking=True)
+            case.k_new[l].copy_(host_k[l], non_blocking=True)
+            case.v_new[l].copy_(host_v[l], non_blocking=True)
+            case.write(l, stream=stream)
+            case.attend(l, stream=stream)
+            host_out[l].copy_(case.out[l], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world) / steps
+    flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * layers * world
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

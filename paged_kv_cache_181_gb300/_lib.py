@@ -1,0 +1,243 @@
+"""ctypes binding of libpagedkv (argument marshalling only).
+
+Every function here converts Python/torch arguments to the C ABI declared in
+include/pagedkv.h and raises on a non-OK status with the library's message.
+No step of the method runs in Python: the host metadata runs in the library's
+C++ and every device step in its CUDA kernels.  When the shared library is
+missing, importing this module raises -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_CHECK, PKV_ERR_CAPACITY = range(6)
+PKV_F32, PKV_BF16, PKV_F16 = 0, 1, 2
+PKV_CHECK_BOUNDS = 0x1
+PKV_FORCE_SIMT = 0x2
+PKV_NO_SPLIT = 0x4
+PKV_SEG_CAUSAL, PKV_SEG_FULL = 0, 1
+PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK, PKV_DEVERR_SEQLEN, PKV_DEVERR_QUERY, PKV_DEVERR_SEGMENT = 1, 2, 4, 8, 16
+
+EXPORTS = (
+    "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
+    "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
+    "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches",
+)
+
+
+def PKV_SPLITS(n: int) -> int:
+    return (int(n) & 0xFF) << 8
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[pkv status {status}] {message}")
+        self.status = status
+
+
+class pkv_segment(C.Structure):
+    _fields_ = [("q_start", C.c_int32), ("q_end", C.c_int32), ("kv_end", C.c_int32), ("mode", C.c_int32)]
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m paged_kv_cache_181_gb300.build` "
+            "(or __graft_entry__.build()) first"
+        )
+    lib = C.CDLL(LIB_PATH)
+    i32p, i64p, vp = C.POINTER(C.c_int32), C.POINTER(C.c_int64), C.c_void_p
+    sig = {
+        "pkv_last_error": (C.c_char_p, []),
+        "pkv_version": (C.c_char_p, []),
+        "build_segments": (C.c_int, [i32p, C.c_int, C.c_int32, C.c_int32, C.c_int32, C.POINTER(pkv_segment), C.c_int,
+                                     C.POINTER(C.c_int)]),
+        "pkv_slot_mapping": (C.c_int, [i32p, C.c_int64, C.c_int64, C.c_int64, C.c_int, i64p]),
+        "pkv_table_width": (C.c_int64, [C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int]),
+        "pkv_visible_window": (C.c_int, [i32p, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int, i32p, C.c_int64,
+                                         i64p, i64p]),
+        "pkv_block_table_row": (C.c_int, [i32p, C.c_int64, C.c_int64, i32p, C.c_int64, C.c_int, C.c_int64, i32p,
+                                          i64p]),
+        "paged_kv_write": (C.c_int, [vp, vp, vp, C.c_int64, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_uint32,
+                                     vp]),
+        "paged_attn_workspace_size": (C.c_size_t, [C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
+        "paged_attn_varlen": (C.c_int, [vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int,
+                                        vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp,
+                                        C.c_size_t, C.c_uint32, vp]),
+        "pkv_check": (C.c_int, [vp, C.POINTER(C.c_uint32)]),
+        "pkv_sm_count": (C.c_int, []),
+        "pkv_last_launches": (C.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.pkv_last_error().decode()
+
+
+def _ok(status: int) -> None:
+    if status != PKV_OK:
+        raise PkvError(status, last_error())
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(arr: np.ndarray, ctype):
+    return arr.ctypes.data_as(C.POINTER(ctype))
+
+
+# ---------------------------------------------------------------- host metadata
+
+
+def build_segments(spans, query_offset: int, query_len: int, seq_len: int) -> list[tuple[int, int, int, int]]:
+    """Segments (q_start, q_end, kv_end, mode) of one row; mode 0 causal, 1 full."""
+    sp = _i32(np.asarray(spans, dtype=np.int64).reshape(-1, 2)) if len(spans) else np.zeros((0, 2), np.int32)
+    cap = 2 * len(spans) + 1
+    out = (pkv_segment * cap)()
+    n = C.c_int(0)
+    _ok(lib.build_segments(_p(sp, C.c_int32), len(spans), int(query_offset), int(query_len), int(seq_len), out, cap,
+                           C.byref(n)))
+    return [(out[i].q_start, out[i].q_end, out[i].kv_end, out[i].mode) for i in range(n.value)]
+
+
+def slot_mapping(blocks, first_position: int, n_tokens: int, block_size: int = 16) -> np.ndarray:
+    b = _i32(blocks)
+    out = np.empty(int(n_tokens), dtype=np.int64)
+    _ok(lib.pkv_slot_mapping(_p(b, C.c_int32), b.size, int(first_position), int(n_tokens), int(block_size),
+                             _p(out, C.c_int64)))
+    return out
+
+
+def table_width(chunk_tokens: int, sink_tokens: int, window_tokens: int, action_len: int, block_size: int = 16) -> int:
+    w = lib.pkv_table_width(int(chunk_tokens), int(sink_tokens), int(window_tokens), int(action_len), int(block_size))
+    if w < 0:
+        raise PkvError(PKV_ERR_INVALID_ARG, last_error())
+    return int(w)
+
+
+def visible_window(row_blocks, end_tokens: int, sink_tokens: int, window_tokens: int, block_size: int = 16):
+    """(visible block ids, video_len) of one row."""
+    rb = _i32(row_blocks)
+    cap = max(1, rb.size)
+    out = np.empty(cap, dtype=np.int32)
+    n = C.c_int64(0)
+    vl = C.c_int64(0)
+    _ok(lib.pkv_visible_window(_p(rb, C.c_int32), rb.size, int(end_tokens), int(sink_tokens), int(window_tokens),
+                               int(block_size), _p(out, C.c_int32), cap, C.byref(n), C.byref(vl)))
+    return out[: n.value].copy(), int(vl.value)
+
+
+def block_table_row(video_blocks, video_len: int, action_blocks, action_len: int, width: int, block_size: int = 16):
+    """(padded int32 row, kv_len)."""
+    vb = _i32(video_blocks)
+    ab = _i32(action_blocks) if len(action_blocks) else np.zeros(1, np.int32)
+    out = np.empty(int(width), dtype=np.int32)
+    kv = C.c_int64(0)
+    _ok(lib.pkv_block_table_row(_p(vb, C.c_int32), vb.size, int(video_len), _p(ab, C.c_int32), int(action_len),
+                                int(block_size), int(width), _p(out, C.c_int32), C.byref(kv)))
+    return out, int(kv.value)
+
+
+# ---------------------------------------------------------------- device ops
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    return {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.float16: PKV_F16}[t.dtype]
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def paged_kv_write(k, v, slot_mapping, key_pool, value_pool, *, flags: int = 0, stream=None) -> None:
+    """key_pool[slot[t]] = k[t]; value_pool[slot[t]] = v[t] (pools ``[num_slots, Hkv, D]``)."""
+    T, hkv, d = k.shape
+    for t in (k, v, key_pool, value_pool):
+        if not t.is_contiguous():
+            raise ValueError("paged_kv_write: tensors must be contiguous")
+    if v.shape != k.shape or key_pool.shape != value_pool.shape or key_pool.shape[1:] != k.shape[1:]:
+        raise ValueError("paged_kv_write: shape mismatch")
+    if k.dtype != key_pool.dtype or v.dtype != value_pool.dtype or k.dtype != v.dtype:
+        raise ValueError("paged_kv_write: sources and pools must share one dtype")
+    if slot_mapping.dtype != _torch().int64 or slot_mapping.numel() != T:
+        raise ValueError("paged_kv_write: slot_mapping must be int64 [T]")
+    _ok(lib.paged_kv_write(_dptr(k), _dptr(v), _dptr(slot_mapping), T, _dptr(key_pool), _dptr(value_pool),
+                           key_pool.shape[0], hkv, d, dtype_code(k), flags, _stream(stream)))
+
+
+def workspace_size(Tq: int, Hq: int, D: int, B: int, max_query_len: int, max_seq_len: int) -> int:
+    return int(lib.paged_attn_workspace_size(int(Tq), int(Hq), int(D), int(B), int(max_query_len), int(max_seq_len)))
+
+
+def paged_attn_varlen(q, key_pool, value_pool, block_table, query_start_loc, seq_lens, max_query_len: int,
+                      max_seq_len: int, softmax_scale: float, *, segs=None, seg_start=None, out=None,
+                      workspace=None, flags: int = 0, block_size: int = 16, stream=None):
+    """Paged varlen attention; pools are ``[num_blocks * 16, Hkv, D]``; returns ``out``."""
+    torch = _torch()
+    Tq, hq, d = q.shape
+    hkv = key_pool.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    for t in (q, key_pool, value_pool, block_table, query_start_loc, seq_lens, out):
+        if not t.is_contiguous():
+            raise ValueError("paged_attn_varlen: tensors must be contiguous")
+    if key_pool.dtype != q.dtype or value_pool.dtype != q.dtype or out.dtype != q.dtype:
+        raise ValueError("paged_attn_varlen: q, pools and out must share one dtype")
+    for t in (block_table, query_start_loc, seq_lens) + ((seg_start,) if seg_start is not None else ()):
+        if t.dtype != torch.int32:
+            raise ValueError("paged_attn_varlen: metadata must be int32")
+    B, W = block_table.shape
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(lib.paged_attn_varlen(_dptr(q), Tq, hq, _dptr(key_pool), _dptr(value_pool), key_pool.shape[0] // block_size,
+                              block_size, hkv, d, dtype_code(q), _dptr(block_table), B, W, _dptr(query_start_loc),
+                              _dptr(seq_lens), int(max_query_len), int(max_seq_len), float(softmax_scale),
+                              _dptr(segs), _dptr(seg_start), _dptr(out), _dptr(workspace), ws, flags,
+                              _stream(stream)))
+    return out
+
+
+def check(stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns its bits (raises PkvError if set)."""
+    bits = C.c_uint32(0)
+    st = lib.pkv_check(_stream(stream), C.byref(bits))
+    if st not in (PKV_OK, PKV_ERR_DEVICE_CHECK):
+        _ok(st)
+    return int(bits.value)
+
+
+def last_launches() -> int:
+    """Kernels launched by the last device call on this thread."""
+    return int(lib.pkv_last_launches())
+
+
+def sm_count() -> int:
+    return int(lib.pkv_sm_count())

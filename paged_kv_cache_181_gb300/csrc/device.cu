@@ -1,0 +1,231 @@
+// Device entry points of libpagedkv: argument validation, key-range split
+// planning, launches, and the device error word read back by pkv_check().
+
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+// One error word per device.  Kernels in PKV_CHECK_BOUNDS mode OR bits into it.
+__device__ unsigned int g_pkv_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::mutex g_mu;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int kMaxSplits = 8;
+
+}  // namespace
+
+unsigned int* pkv_device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = (unsigned int*)p;
+  }
+  return g_err_ptr[dev];
+}
+
+extern "C" int pkv_sm_count(void) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sm_count[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+extern "C" pkv_status pkv_check(void* stream, uint32_t* bits) {
+  pkv_clear_error();
+  if (bits) *bits = 0;
+  unsigned int* w = pkv_device_error_word();
+  if (!w) return pkv_fail(PKV_ERR_CUDA, "pkv_check: no CUDA device");
+  unsigned int host = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&host, w, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof(unsigned int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return pkv_fail(PKV_ERR_CUDA, "pkv_check: %s", cudaGetErrorString(e));
+  if (bits) *bits = host;
+  if (host) return pkv_fail(PKV_ERR_DEVICE_CHECK, "pkv_check: device metadata check failed (bits 0x%x)", host);
+  return PKV_OK;
+}
+
+extern "C" pkv_status paged_kv_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T,
+                                     void* key_pool, void* value_pool, int64_t num_slots, int Hkv, int D,
+                                     pkv_dtype dt, uint32_t flags, void* stream) {
+  pkv_clear_error();
+  pkv_set_launches(0);
+  if (T < 0 || num_slots < 0 || Hkv <= 0 || D <= 0)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_write: negative or zero size (T=%lld, Hkv=%d, D=%d)",
+                    (long long)T, Hkv, D);
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_kv_write: unknown dtype %d", (int)dt);
+  if (T == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !key_pool || !value_pool)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_write: NULL pointer");
+  const int64_t row_bytes = (int64_t)Hkv * D * pkv_dtype_size(dt);
+  if (row_bytes % 16 || !aligned16(k) || !aligned16(v) || !aligned16(key_pool) || !aligned16(value_pool))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_write: rows (%lld bytes) and base pointers must be 16-byte aligned",
+                    (long long)row_bytes);
+  if (row_bytes / 16 > (1 << 30)) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_kv_write: row too large");
+  const int check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
+  unsigned int* err = check ? pkv_device_error_word() : nullptr;
+  if (check && !err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: device error word unavailable");
+  const int rc = pkv_launch_kv_write(k, v, slot_mapping, T, key_pool, value_pool, num_slots, (int)row_bytes, err,
+                                     check, stream);
+  if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+  pkv_set_launches(1);
+  return PKV_OK;
+}
+
+namespace {
+
+// Split the key range only when the grid would otherwise leave SMs idle.
+// `units` = CTAs the unsplit launch has; `tiles` = key tiles per unit.
+int plan_splits(int64_t units, int64_t tiles, int sms, int max_splits) {
+  if (units <= 0 || tiles <= 1) return 1;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int64_t per = (tiles + s - 1) / s;
+    if (s > 1 && per < 4) break;  // too little work per split
+    const int64_t ctas = units * s;
+    const int64_t waves = (ctas + sms - 1) / sms;
+    // cost model: waves x per-split length, plus a small charge per split for the combine
+    const double cost = (double)waves * (double)(per + 2) + 0.02 * s * (double)tiles;
+    if (cost < best_cost * 0.97) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+extern "C" size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len) {
+  (void)B;
+  (void)max_query_len;
+  (void)max_seq_len;
+  if (Tq <= 0 || Hq <= 0 || D <= 0) return 0;
+  return (size_t)kMaxSplits * (size_t)Tq * (size_t)Hq * ((size_t)D + 1) * sizeof(float);
+}
+
+extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const void* key_pool,
+                                        const void* value_pool, int64_t num_blocks, int block_size, int Hkv, int D,
+                                        pkv_dtype dt, const int32_t* block_table, int B, int W,
+                                        const int32_t* query_start_loc, const int32_t* seq_lens, int max_query_len,
+                                        int max_seq_len, float softmax_scale, const pkv_segment* segs,
+                                        const int32_t* seg_start, void* out, void* workspace, size_t ws_bytes,
+                                        uint32_t flags, void* stream) {
+  pkv_clear_error();
+  pkv_set_launches(0);
+  if (Tq < 0 || B < 0 || W < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: negative size");
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv)
+    return pkv_fail(PKV_ERR_INVALID_ARG,
+                    "paged_attn_varlen: num_heads must be a positive multiple of num_kv_heads (Hq=%d, Hkv=%d)", Hq, Hkv);
+  if (block_size != 16) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: block_size must be 16 (got %d)", block_size);
+  if (D != 64 && D != 128) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: head dim must be 64 or 128 (got %d)", D);
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: unknown dtype %d", (int)dt);
+  if (!isfinite(softmax_scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: softmax_scale is not finite");
+  if ((int64_t)max_seq_len > (int64_t)W * block_size)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: max_seq_len %d exceeds the table's %d x %d slots",
+                    max_seq_len, W, block_size);
+  if (Tq == 0 || B == 0 || max_query_len == 0) return PKV_OK;
+  if (!q || !key_pool || !value_pool || !block_table || !query_start_loc || !seq_lens || !out)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: NULL pointer");
+  if (segs && !seg_start) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: segs given without seg_start");
+  if (!aligned16(q) || !aligned16(key_pool) || !aligned16(value_pool) || !aligned16(out))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: q, pools and out must be 16-byte aligned");
+  if (max_query_len > max_seq_len)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: max_query_len %d > max_seq_len %d (the query is a "
+                    "suffix of the key sequence)", max_query_len, max_seq_len);
+
+  PkvAttnArgs a{};
+  a.q = q;
+  a.k_pool = key_pool;
+  a.v_pool = value_pool;
+  a.out = out;
+  a.block_table = block_table;
+  a.query_start_loc = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.segs = segs;
+  a.seg_start = seg_start;
+  a.num_blocks = num_blocks;
+  a.Tq = Tq;
+  a.B = B;
+  a.W = W;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
+  a.scale = softmax_scale;
+  a.check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
+  a.err = a.check ? pkv_device_error_word() : nullptr;
+  if (a.check && !a.err) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: device error word unavailable");
+
+  const bool use_tc = !(flags & PKV_FORCE_SIMT) && pkv_attn_tc_supports(dt, D);
+  int sms = pkv_sm_count();
+  if (sms <= 0) sms = 152;
+
+  // Split planning from host-visible sizes only.
+  int forced = (int)((flags >> 8) & 0xffu);
+  int splits = 1;
+  if (forced > 0) {
+    splits = forced > kMaxSplits ? kMaxSplits : forced;
+  } else if (!(flags & PKV_NO_SPLIT) && workspace && ws_bytes) {
+    const int64_t q_tile = use_tc ? 128 : 16;
+    const int64_t k_tile = use_tc ? 128 : 32;
+    const int64_t units = (int64_t)B * Hq * ((max_query_len + q_tile - 1) / q_tile);
+    const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
+    splits = plan_splits(units, tiles, use_tc ? sms : sms * 8, kMaxSplits);
+  }
+  if (splits > 1) {
+    const size_t need = (size_t)splits * (size_t)Tq * Hq * ((size_t)D + 1) * sizeof(float);
+    if (!workspace || ws_bytes < need) {
+      if (forced > 0)
+        return pkv_fail(PKV_ERR_CAPACITY, "paged_attn_varlen: %d splits need %zu workspace bytes, got %zu", splits,
+                        need, ws_bytes);
+      splits = 1;
+    } else {
+      if (!aligned16(workspace)) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: workspace must be 16-byte aligned");
+      a.part_o = (float*)workspace;
+      a.part_lse = a.part_o + (size_t)splits * Tq * Hq * D;
+    }
+  }
+  a.num_splits = splits;
+
+  int rc = -1;
+  if (use_tc) rc = pkv_launch_attn_tc(a, dt, stream);
+  if (rc == -1) rc = pkv_launch_attn_simt(a, dt, stream);
+  if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+  if (splits > 1) {
+    rc = pkv_launch_attn_combine(a, dt, stream);
+    if (rc != 0)
+      return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: combine launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+  }
+  pkv_set_launches(splits > 1 ? 2 : 1);
+  return PKV_OK;
+}

@@ -1,0 +1,49 @@
+// Declarations shared by the translation units of libpagedkv (not installed).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+// Record a failure message for pkv_last_error() and return `code`.
+pkv_status pkv_fail(pkv_status code, const char* fmt, ...);
+void pkv_clear_error();
+void pkv_set_launches(int n);
+
+// Device error word of the current device (PKV_DEVERR_* bits); nullptr when unavailable.
+unsigned int* pkv_device_error_word();
+
+inline int pkv_dtype_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
+
+// Per-row work description shared by the attention kernels.
+struct PkvAttnArgs {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  void* out;
+  const int32_t* block_table;
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  const pkv_segment* segs;
+  const int32_t* seg_start;
+  float* part_o;    // [splits, Tq, Hq, D] fp32, when splitting
+  float* part_lse;  // [splits, Tq, Hq] fp32 (natural log), when splitting
+  unsigned int* err;
+  int64_t num_blocks;
+  int64_t Tq;
+  int B, W, Hq, Hkv, D;
+  int max_query_len, max_seq_len;
+  int num_splits;
+  int check;
+  float scale;
+};
+
+// Launchers (each returns cudaGetLastError() as an int, 0 == success).
+int pkv_launch_kv_write(const void* k, const void* v, const int64_t* slots, int64_t T, void* kp, void* vp,
+                        int64_t num_slots, int row_bytes, unsigned int* err, int check, void* stream);
+int pkv_launch_attn_simt(const PkvAttnArgs& a, pkv_dtype dt, void* stream);
+int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream);
+// tcgen05 path; returns -1 when the shape is not handled by it.
+int pkv_launch_attn_tc(const PkvAttnArgs& a, pkv_dtype dt, void* stream);
+bool pkv_attn_tc_supports(pkv_dtype dt, int D);

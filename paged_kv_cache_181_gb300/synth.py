@@ -1,17 +1,19 @@
 """Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
 
-This module holds random draws only -- no arithmetic of the method.  One
-``torch.Generator`` per (workload, layer) draws, in this order:
+This module holds random draws only -- no arithmetic of the method.
 
-1. the pool permutation (block allocation): every row gets ``ceil(end / bs)``
-   logical blocks for its video positions, then ``ceil(action_len / bs)``
-   scratch blocks for its action tokens, taken in turn from a random
-   permutation of blocks ``1 .. pool_blocks-1``.  Block 0 is never handed out:
-   it is the table's padding entry, so a test can poison it;
-2. Q ``[B * q_len, Hq, D]`` ~ N(0, sigma);
-3. history K, V ``[B, history, Hkv, D]`` ~ N(0, sigma);
-4. current K, V ``[B * q_len, Hkv, D]`` ~ N(0, sigma) (video tokens, then the
-   row's action tokens).
+* Block allocation (one per workload, shared by every layer, as the layers of
+  one forward share one block table): a CPU ``torch.Generator`` seeded
+  ``seed * 1000 + 999`` draws a random permutation of blocks
+  ``1 .. pool_blocks-1``; each row in turn takes ``ceil(end / bs)`` blocks for
+  its video positions, then ``ceil(action_len / bs)`` scratch blocks for its
+  action tokens.  Block 0 is never handed out: it is the table's padding
+  entry, so a test can poison it.
+* Layer data: a ``torch.Generator`` on the requested device seeded
+  ``seed * 1000 + layer`` draws, in order, Q ``[B * q_len, Hq, D]``, history K
+  and V ``[B, history, Hkv, D]``, and the current chunk's K and V
+  ``[B * q_len, Hkv, D]`` (each row's video tokens, then its action tokens),
+  all ~ N(0, sigma).
 
 Values are drawn in float32 and rounded to the workload dtype
 (round-to-nearest-even), so the oracle can upcast the exact same numbers.
@@ -49,25 +51,32 @@ def seed_of(w: Workload, layer: int) -> int:
     return w.seed * 1000 + layer
 
 
-def draw(w: Workload, layer: int = 0, device="cpu") -> Draw:
-    """Draw one layer's inputs for workload ``w`` on ``device``."""
-    dev = torch.device(device)
-    g = torch.Generator(device=dev)
-    g.manual_seed(seed_of(w, layer))
-    dt = TORCH_DTYPE[w.dtype]
+def allocation(w: Workload):
+    """(row_blocks, action_blocks): per row, int64 tensors of physical block ids."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed * 1000 + 999)
     bs = w.block_size
     n_video = _ceil_div(w.end_tokens, bs)
     n_action = _ceil_div(w.action_len, bs)
     per_row = n_video + n_action
     if w.batch * per_row > w.pool_blocks - 1:
         raise ValueError(f"{w.name}: pool of {w.pool_blocks} blocks cannot hold {w.batch} rows of {per_row}")
-    perm = torch.randperm(w.pool_blocks - 1, generator=g, device=dev) + 1
-    perm = perm.to("cpu", torch.int64)
+    perm = torch.randperm(w.pool_blocks - 1, generator=g) + 1
     row_blocks, action_blocks = [], []
     for b in range(w.batch):
         base = b * per_row
         row_blocks.append(perm[base : base + n_video].clone())
         action_blocks.append(perm[base + n_video : base + per_row].clone())
+    return row_blocks, action_blocks
+
+
+def draw(w: Workload, layer: int = 0, device="cpu") -> Draw:
+    """Draw one layer's inputs for workload ``w`` on ``device``."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed_of(w, layer))
+    dt = TORCH_DTYPE[w.dtype]
+    row_blocks, action_blocks = allocation(w)
 
     def normal(*shape):
         x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)

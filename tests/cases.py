@@ -1,0 +1,103 @@
+"""Oracle side of a workload: metadata, pools and expected outputs from oracle/ only.
+
+Uses the shared seeded draws (paged_kv_cache_181_gb300.synth) and nothing of
+the CUDA path.  Pools are float32 (bf16/f16 values are exact in float32) and
+poisoned with NaN, so any read of a slot that was never written shows up.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from oracle import pagedattn as pa
+from oracle import window as ow
+from paged_kv_cache_181_gb300 import synth
+from paged_kv_cache_181_gb300.configs import Workload
+
+
+@dataclass
+class OracleCase:
+    table: np.ndarray
+    seq_lens: np.ndarray
+    qsl: np.ndarray
+    slots: np.ndarray
+    segments: list | None
+    width: int
+    k_pool: np.ndarray | None = None
+    v_pool: np.ndarray | None = None
+    q: np.ndarray | None = None
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def oracle_metadata(w: Workload) -> OracleCase:
+    row_blocks, action_blocks = synth.allocation(w)
+    bs = w.block_size
+    width = ow.table_width(w.chunk_tokens, bs, w.sink_tokens, w.window_tokens, w.action_len)
+    table = np.zeros((w.batch, width), dtype=np.int64)
+    seq_lens = np.zeros(w.batch, dtype=np.int64)
+    qsl = np.arange(w.batch + 1, dtype=np.int64) * w.q_len
+    slots, segments = [], ([] if w.spans else None)
+    for b in range(w.batch):
+        rb = [int(x) for x in row_blocks[b]]
+        ab = [int(x) for x in action_blocks[b]]
+        blocks, video_len = ow.visible_video_blocks(rb, w.end_tokens, w.sink_tokens, w.window_tokens, bs)
+        row, kv_len = ow.block_table_row(blocks, video_len, ab, w.action_len, bs, width)
+        table[b] = row
+        seq_lens[b] = kv_len
+        slots.append(pa.slot_mapping(rb, range(w.history_tokens, w.end_tokens), bs))
+        if w.action_len:
+            slots.append(pa.slot_mapping(ab, range(w.action_len), bs))
+        if segments is not None:
+            pa.validate_spans(list(w.spans), kv_len - w.q_len, w.q_len, kv_len)
+            segments.append(pa.build_segments(list(w.spans), kv_len - w.q_len, w.q_len))
+    return OracleCase(table, seq_lens, qsl, np.concatenate(slots), segments, width)
+
+
+def oracle_pools(w: Workload, d: synth.Draw, oc: OracleCase) -> None:
+    """Write history and the current chunk into NaN-poisoned float32 pools."""
+    row_blocks, _ = synth.allocation(w)
+    n_slots = w.pool_blocks * w.block_size
+    kp = np.full((n_slots, w.num_kv_heads, w.head_dim), np.nan, dtype=np.float32)
+    vp = np.full_like(kp, np.nan)
+    for b in range(w.batch):
+        hs = pa.slot_mapping([int(x) for x in row_blocks[b]], range(w.history_tokens), w.block_size)
+        pa.kv_write(kp, hs, to_np(d.k_hist[b]))
+        pa.kv_write(vp, hs, to_np(d.v_hist[b]))
+    pa.kv_write(kp, oc.slots, to_np(d.k_cur))
+    pa.kv_write(vp, oc.slots, to_np(d.v_cur))
+    oc.k_pool, oc.v_pool, oc.q = kp, vp, to_np(d.q)
+
+
+def expected(w: Workload, oc: OracleCase, sample=None) -> np.ndarray:
+    return pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, w.head_dim ** -0.5,
+                              w.block_size, oc.segments, sample=sample)
+
+
+def sample_rows(w: Workload, per_head: int, seed: int = 0) -> dict:
+    """Sampled local query rows per (row, head): first and last rows, the tail tile, and random ones."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for b in range(w.batch):
+        for h in range(w.num_heads):
+            fixed = {0, w.q_len - 1, max(0, w.q_len - 24), w.query_tokens - 1, min(w.q_len - 1, w.query_tokens)}
+            extra = rng.choice(w.q_len, size=min(per_head, w.q_len), replace=False)
+            out[(b, h)] = np.array(sorted(fixed | set(int(x) for x in extra)), dtype=np.int64)
+    return out
+
+
+def compare(got: np.ndarray, want: np.ndarray, dtype: str, mask=None) -> tuple[float, float]:
+    """(max-abs, mean-abs) error over the compared entries; NaN anywhere in got fails."""
+    if mask is not None:
+        got, want = got[mask], want[mask]
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got.astype(np.float64) - want)
+    return float(err.max()), float(err.mean())
+
+
+TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 2e-3), "f16": (2e-2, 2e-3)}

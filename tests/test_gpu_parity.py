@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by element.
+
+The write and the host metadata must be bit-exact; attention must be within
+max-abs 2e-2 / mean-abs 2e-3 of the float64 oracle for bf16/f16 inputs and
+within 1e-4 for fp32.  Pools are NaN-poisoned, so reading any unwritten slot,
+the evicted gap between the sink and the window, or table padding (block 0,
+never allocated) turns an output NaN and fails.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_181_gb300 import configs
+
+from . import cases
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [configs.TINY, configs.ONE_FRAME, configs.ONE_FRAME_PARTIAL, configs.GQA_ACTION, configs.MIXED_MASK]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_181_gb300 import _lib
+
+    return _lib
+
+
+def run_case(w, flags=0, poison=True):
+    from paged_kv_cache_181_gb300 import workload
+
+    case = workload.build_case(w, poison=poison, keep_draws=True, layers=1)
+    case.write(0, flags)
+    out = case.attend(0, flags)
+    torch.cuda.synchronize()
+    return case, out
+
+
+def check_metadata(case, oc):
+    assert np.array_equal(case.meta.table, oc.table)
+    assert np.array_equal(case.meta.seq_lens, oc.seq_lens)
+    assert np.array_equal(case.meta.query_start_loc, oc.qsl)
+    assert np.array_equal(case.meta.slots, oc.slots)
+    if oc.segments is None:
+        assert case.meta.segments is None
+    else:
+        want = [[(s.q_start, s.q_end, s.kv_end, 0 if s.mode == "causal" else 1) for s in row] for row in oc.segments]
+        assert case.meta.segments == want
+
+
+def check_pools(case, oc):
+    # Bit-exact write: every slot equals the oracle's (NaN where never written).
+    for gpu_pool, want in ((case.k_pools[0], oc.k_pool), (case.v_pools[0], oc.v_pool)):
+        got = gpu_pool.float().cpu().numpy()
+        both_nan = np.isnan(got) & np.isnan(want)
+        assert (both_nan | (got == want)).all()
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_workload_parity(lib, w):
+    case, out = run_case(w)
+    oc = cases.oracle_metadata(w)
+    check_metadata(case, oc)
+    cases.oracle_pools(w, case.draws[0], oc)
+    check_pools(case, oc)
+    full = w.batch * w.q_len * w.num_heads * w.q_len <= 2_000_000 or w.name == "one-frame-bf16"
+    sample = None if full else cases.sample_rows(w, 48)
+    want = cases.expected(w, oc, sample)
+    got = out.float().cpu().numpy()
+    mask = None if sample is None else ~np.isnan(want)
+    max_abs, mean_abs = cases.compare(got, want, w.dtype, mask)
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("w", [configs.GQA_ACTION, configs.ONE_FRAME_PARTIAL], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", ["splits3", "simt", "nosplit"])
+def test_variants_agree(lib, w, mode):
+    flags = {"splits3": lib.PKV_SPLITS(3), "simt": lib.PKV_FORCE_SIMT, "nosplit": lib.PKV_NO_SPLIT}[mode]
+    case, out = run_case(w, flags)
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, case.draws[0], oc)
+    sample = cases.sample_rows(w, 16, seed=3)
+    want = cases.expected(w, oc, sample)
+    max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
+
+
+def test_repeat_runs_are_bit_identical(lib):
+    w = configs.MIXED_MASK
+    case, out1 = run_case(w, poison=False)
+    out1 = out1.clone()
+    out2 = case.attend(0).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+EDGE = [
+    # D=64 bf16, GQA 3, ragged query tail, window + sink, action tokens
+    dataclasses.replace(configs.GQA_ACTION, name="edge-d64", num_heads=6, num_kv_heads=2, head_dim=64,
+                        chunk_tokens=200, window_chunks=2, sink_chunks=1, history_tokens=600, query_tokens=200,
+                        action_len=20, spans=((1000, 1200),), pool_blocks=512, seed=21),
+    # fp16, a single query token over a partial block
+    dataclasses.replace(configs.ONE_FRAME, name="edge-f16-1tok", dtype="f16", num_heads=4, num_kv_heads=4,
+                        chunk_tokens=1, window_chunks=40, sink_chunks=0, history_tokens=36, query_tokens=1,
+                        pool_blocks=64, seed=22),
+    # one key in total
+    dataclasses.replace(configs.TINY, name="edge-one-key", chunk_tokens=1, window_chunks=1, history_tokens=0,
+                        query_tokens=1, seed=23),
+    # fp32, MHA, causal-only mask via a span that misses the query
+    dataclasses.replace(configs.TINY, name="edge-f32-causal", history_tokens=40, query_tokens=40, chunk_tokens=40,
+                        window_chunks=2, spans=((0, 8),), pool_blocks=64, seed=24),
+    # bf16, batch 1, query tile boundary (exactly 256 queries)
+    dataclasses.replace(configs.ONE_FRAME, name="edge-b1-256", batch=1, num_heads=2, num_kv_heads=1,
+                        chunk_tokens=256, window_chunks=3, sink_chunks=0, history_tokens=512, query_tokens=256,
+                        pool_blocks=128, seed=25),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
+def test_edge_cases(lib, w):
+    case, out = run_case(w)
+    oc = cases.oracle_metadata(w)
+    check_metadata(case, oc)
+    cases.oracle_pools(w, case.draws[0], oc)
+    check_pools(case, oc)
+    want = cases.expected(w, oc)
+    max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype)
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
