@@ -133,7 +133,7 @@ def build_case(w: Workload, device="cuda", layers: int | None = None, poison: bo
         starts = np.concatenate([[0], np.cumsum([len(r) for r in meta.segments])]).astype(np.int32)
         segs = _pinned_to(np.asarray(flat, dtype=np.int32).reshape(-1, 4), dev)
         seg_start = _pinned_to(starts, dev)
-    hist_slots = [_pinned_to(s, dev) for s in meta.hist_slots]
+    hist_slots = [_pinned_to(s, dev) for s in meta.history_slots]
     k_pools, v_pools, qs, ks, vs, outs, draws = [], [], [], [], [], [], []
     for layer in range(n_layers):
         d = synth.draw(w, layer, device=data_device)

@@ -7,6 +7,7 @@ poisoned with NaN, so any read of a slot that was never written shows up.
 
 from __future__ import annotations
 
+import dataclasses
 from dataclasses import dataclass
 
 import numpy as np
@@ -14,7 +15,7 @@ import torch
 
 from oracle import pagedattn as pa
 from oracle import window as ow
-from paged_kv_cache_181_gb300 import synth
+from paged_kv_cache_181_gb300 import configs, synth
 from paged_kv_cache_181_gb300.configs import Workload
 
 
@@ -101,3 +102,27 @@ def compare(got: np.ndarray, want: np.ndarray, dtype: str, mask=None) -> tuple[f
 
 
 TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 2e-3), "f16": (2e-2, 2e-3)}
+
+
+# Small workloads covering edge cases: D=64, GQA 3, ragged tails, fp16, a single query, a single key,
+# causal-only masks, batch 1 with an exact 256-query tile boundary.
+EDGE = [
+    # D=64 bf16, GQA 3, ragged query tail, window + sink, action tokens
+    dataclasses.replace(configs.GQA_ACTION, name="edge-d64", num_heads=6, num_kv_heads=2, head_dim=64,
+                        chunk_tokens=200, window_chunks=2, sink_chunks=1, history_tokens=600, query_tokens=200,
+                        action_len=20, spans=((408, 608),), pool_blocks=512, seed=21),
+    # fp16, a single query token over a partial block
+    dataclasses.replace(configs.ONE_FRAME, name="edge-f16-1tok", dtype="f16", num_heads=4, num_kv_heads=4,
+                        chunk_tokens=1, window_chunks=40, sink_chunks=0, history_tokens=36, query_tokens=1,
+                        pool_blocks=64, seed=22),
+    # one key in total
+    dataclasses.replace(configs.TINY, name="edge-one-key", chunk_tokens=1, window_chunks=1, history_tokens=0,
+                        query_tokens=1, seed=23),
+    # fp32, MHA, causal-only mask via a span that misses the query
+    dataclasses.replace(configs.TINY, name="edge-f32-causal", history_tokens=40, query_tokens=40, chunk_tokens=40,
+                        window_chunks=2, spans=((0, 8),), pool_blocks=64, seed=24),
+    # bf16, batch 1, query tile boundary (exactly 256 queries)
+    dataclasses.replace(configs.ONE_FRAME, name="edge-b1-256", batch=1, num_heads=2, num_kv_heads=1,
+                        chunk_tokens=256, window_chunks=3, sink_chunks=0, history_tokens=512, query_tokens=256,
+                        pool_blocks=128, seed=25),
+]

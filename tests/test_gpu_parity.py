@@ -100,26 +100,7 @@ def test_repeat_runs_are_bit_identical(lib):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-EDGE = [
-    # D=64 bf16, GQA 3, ragged query tail, window + sink, action tokens
-    dataclasses.replace(configs.GQA_ACTION, name="edge-d64", num_heads=6, num_kv_heads=2, head_dim=64,
-                        chunk_tokens=200, window_chunks=2, sink_chunks=1, history_tokens=600, query_tokens=200,
-                        action_len=20, spans=((1000, 1200),), pool_blocks=512, seed=21),
-    # fp16, a single query token over a partial block
-    dataclasses.replace(configs.ONE_FRAME, name="edge-f16-1tok", dtype="f16", num_heads=4, num_kv_heads=4,
-                        chunk_tokens=1, window_chunks=40, sink_chunks=0, history_tokens=36, query_tokens=1,
-                        pool_blocks=64, seed=22),
-    # one key in total
-    dataclasses.replace(configs.TINY, name="edge-one-key", chunk_tokens=1, window_chunks=1, history_tokens=0,
-                        query_tokens=1, seed=23),
-    # fp32, MHA, causal-only mask via a span that misses the query
-    dataclasses.replace(configs.TINY, name="edge-f32-causal", history_tokens=40, query_tokens=40, chunk_tokens=40,
-                        window_chunks=2, spans=((0, 8),), pool_blocks=64, seed=24),
-    # bf16, batch 1, query tile boundary (exactly 256 queries)
-    dataclasses.replace(configs.ONE_FRAME, name="edge-b1-256", batch=1, num_heads=2, num_kv_heads=1,
-                        chunk_tokens=256, window_chunks=3, sink_chunks=0, history_tokens=512, query_tokens=256,
-                        pool_blocks=128, seed=25),
-]
+EDGE = cases.EDGE
 
 
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
