@@ -339,7 +339,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "simt-v0"
+KERNEL_REV = "tc-v1"
 
 
 def run_e2e(case, args, world, stream):

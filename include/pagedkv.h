@@ -82,6 +82,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 #define PKV_DEVERR_SEQLEN 0x4u    /* seq_lens[b] > W * block_size or > max_seq_len, or Sq > seq_len */
 #define PKV_DEVERR_QUERY 0x8u     /* query_start_loc not monotone, or Sq > max_query_len */
 #define PKV_DEVERR_SEGMENT 0x10u  /* a segment outside the row's query range, or a query row no segment covers */
+#define PKV_DEVERR_TIMEOUT 0x20u  /* a pipeline wait inside a kernel gave up (the kernel unwound; results invalid) */
 
 /*
  * One piece of a piecewise causal/full mask, in GLOBAL key coordinates

@@ -24,6 +24,7 @@ PKV_FORCE_SIMT = 0x2
 PKV_NO_SPLIT = 0x4
 PKV_SEG_CAUSAL, PKV_SEG_FULL = 0, 1
 PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK, PKV_DEVERR_SEQLEN, PKV_DEVERR_QUERY, PKV_DEVERR_SEGMENT = 1, 2, 4, 8, 16
+PKV_DEVERR_TIMEOUT = 32
 
 EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",

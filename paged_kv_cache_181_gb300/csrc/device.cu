@@ -183,8 +183,9 @@ extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const
   a.max_seq_len = max_seq_len;
   a.scale = softmax_scale;
   a.check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
-  a.err = a.check ? pkv_device_error_word() : nullptr;
-  if (a.check && !a.err) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: device error word unavailable");
+  // The error word is always passed: the tensor-core kernel reports pipeline timeouts through it.
+  a.err = pkv_device_error_word();
+  if (!a.err) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: device error word unavailable");
 
   const bool use_tc = !(flags & PKV_FORCE_SIMT) && pkv_attn_tc_supports(dt, D);
   int sms = pkv_sm_count();

@@ -100,6 +100,7 @@ def test_long_window_forty_layers_full_size(lib):
     case = workload.build_case(w, device="cuda", poison=False)
     case.step()
     torch.cuda.synchronize()
+    assert lib.check() == 0
     oc0 = cases.oracle_metadata(w)
     assert np.array_equal(case.meta.table, oc0.table) and np.array_equal(case.meta.seq_lens, oc0.seq_lens)
     assert int(oc0.seq_lens[0]) == 26520

@@ -36,6 +36,9 @@ def run_case(w, flags=0, poison=True):
     case.write(0, flags)
     out = case.attend(0, flags)
     torch.cuda.synchronize()
+    from paged_kv_cache_181_gb300 import _lib
+
+    assert _lib.check() == 0, "device error word set"
     return case, out
 
 
