@@ -406,7 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       float o[D];
       if (n > 0) {
-        if (__all_sync(0xffffffffu, ptx::mbar_wait(&sm.o_done, (n - 1) & 1, &sm.abort, kWaitLimitNs))) {
+        // Not o_done: when the last tile is reached that barrier can still be two
+        // phases behind (P.V of tile n-2 in flight), and a parity wait would then
+        // pass at once.  mma_done completes exactly once, after every MMA.
+        if (__all_sync(0xffffffffu, ptx::mbar_wait(&sm.mma_done, 0, &sm.abort, kWaitLimitNs))) {
           ptx::tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
