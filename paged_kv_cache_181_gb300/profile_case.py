@@ -1,0 +1,40 @@
+"""Run a few forwards of one workload for a profiler to capture.
+
+    python -m paged_kv_cache_181_gb300.profile_case --workload long-window-40L-bf16 --layers 1 --steps 3
+
+Builds the workload's pools and metadata like the benchmark does (with
+``--layers`` layers instead of the workload's own count, to keep a capture
+small), runs ``--steps`` forwards -- each layer: KV write, then paged
+attention -- and checks the device error word.  It prints nothing of the
+timing: numbers taken under a profiler are not benchmark figures.
+"""
+
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import _lib, configs, workload
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="long-window-40L-bf16")
+    ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--flags", type=int, default=0)
+    args = ap.parse_args()
+    w = configs.ALL[args.workload]
+    case = workload.build_case(w, device="cuda", layers=args.layers, data_device="cuda")
+    for _ in range(args.steps):
+        case.step(flags=args.flags)
+    torch.cuda.synchronize()
+    bits = _lib.check()
+    if bits:
+        raise SystemExit(f"device error word 0x{bits:x}")
+    print(f"profile_case: {w.name}, {args.layers} layer(s), {args.steps} forward(s): ok")
+
+
+if __name__ == "__main__":
+    main()
