@@ -339,7 +339,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v1"
+KERNEL_REV = "tc-v2-blockbox"
 
 
 def run_e2e(case, args, world, stream):

@@ -10,8 +10,16 @@
 // One CTA = 128 queries of one (row, query head) and one key-range split.
 // Warp roles (192 threads):
 //   warp 0     producer: gathers 128-key K and V tiles through the block table
-//              with TMA, one 16-row box per pool block and 64-column half of
-//              the head (128-byte swizzle), into a 3-stage ring per operand;
+//              with TMA, ONE box per 16-row pool block (4 KB for D=128): the
+//              pool is viewed as a 5-D tensor (64 columns, 8 rows, D/64
+//              column halves, row groups of 8, heads) so that a box lands as
+//              [block][row group][column half][8 rows][128 B], 128-byte
+//              swizzled.  Every 8-row x 128-byte atom then sits at a uniform
+//              stride (GS = D/64 KB) in both the key and the value tile, which
+//              is what the K-major (Q K^T) and MN-major (P V) shared-memory
+//              descriptors need.  (Two 2 KB boxes per block -- one per column
+//              half -- measured about half the load rate.)  3-stage ring per
+//              operand; a partly written last block is loaded row by row;
 //   warp 1     MMA issuer (one thread): S = Q K^T (Q from TMEM, K from shared
 //              memory) into one of two TMEM score buffers, then O += P V (P from
 //              TMEM, V from shared memory, MN-major) into the TMEM output;
@@ -54,8 +62,15 @@ struct alignas(1024) TcSmem {
 };
 
 struct TcMaps {
-  CUtensorMap k16, v16, k1, v1;  // 16-row boxes (whole blocks) and 1-row boxes (partial blocks)
+  CUtensorMap kb, vb;  // 5-D views, box = one whole pool block of one head
+  CUtensorMap k1, v1;  // 3-D views (D, Hkv, slots), box = 64 columns of one row (partial blocks)
 };
+
+// Tile layout: byte offset of 128-byte row (tile row r, column half dh).
+template <int D>
+__host__ __device__ constexpr int tile_row_offset(int r, int dh) {
+  return (r >> 4) * (2 * (D / 64) * 1024) + ((r >> 3) & 1) * ((D / 64) * 1024) + dh * 1024 + (r & 7) * 128;
+}
 
 template <int D>
 PKV_DEVINLINE void note_abort(TcSmem<D>& sm, unsigned int* err) {
@@ -72,7 +87,7 @@ PKV_DEVINLINE bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort
 
 // Producer: gather key rows [j0, j0 + rows) of one (row, kv head) into a stage.
 template <int D>
-PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* m16, const CUtensorMap* m1, uint64_t* full,
+PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensorMap* m1, uint64_t* full,
                              const PkvAttnArgs& a, int b, int kvh, int kt, int rows, int lane) {
   const int n_pages = (rows + 15) >> 4;
   const int rem = rows & 15;
@@ -86,14 +101,13 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* m16, const CUtenso
       blk = 0;
     }
     const bool partial = (p == n_pages - 1) && rem != 0;
+    if (!partial) {
+      ptx::tma_load_5d(dst + tile_row_offset<D>(p * 16, 0), mb, 0, 0, 0, blk * 2, kvh, full);
+    } else {
+      for (int r = 0; r < rem; ++r)
 #pragma unroll
-    for (int dh = 0; dh < D / 64; ++dh) {
-      uint8_t* base = dst + dh * (BN * 128) + p * 16 * 128;
-      if (!partial) {
-        ptx::tma_load_3d(base, m16, dh * 64, kvh, blk * 16, full);
-      } else {
-        for (int r = 0; r < rem; ++r) ptx::tma_load_3d(base + r * 128, m1, dh * 64, kvh, blk * 16 + r, full);
-      }
+        for (int dh = 0; dh < D / 64; ++dh)
+          ptx::tma_load_3d(dst + tile_row_offset<D>(p * 16 + r, dh), m1, dh * 64, kvh, blk * 16 + r, full);
     }
   }
 }
@@ -158,8 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&maps.k16);
-    ptx::prefetch_tmap(&maps.v16);
+    ptx::prefetch_tmap(&maps.kb);
+    ptx::prefetch_tmap(&maps.vb);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -216,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) note_abort(sm, a.err);
         break;
       }
-      load_tile<D>(sm.k[st], &maps.k16, &maps.k1, &sm.k_full[st], a, b, kvh, kt, rows, lane);
+      load_tile<D>(sm.k[st], &maps.kb, &maps.k1, &sm.k_full[st], a, b, kvh, kt, rows, lane);
       if (j >= NST && !warp_wait(&sm.v_empty[st], (use - 1) & 1, &sm.abort, lane)) {
         if (lane == 0) note_abort(sm, a.err);
         issued = j;  // K of tile j is in flight
@@ -226,16 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Key rows past the last visible key are never loaded: zero them in V
         // (P is 0 there, but 0 * NaN would not be).  Zeroing whole 128-byte
         // rows is independent of the swizzle.
-        uint4* vz = reinterpret_cast<uint4*>(sm.v[st]);
-        const int nz = (BN - rows) * 8;  // 16-byte chunks per d-half
-        for (int e = lane; e < nz * (D / 64); e += 32) {
-          const int dh = e / nz, c = e % nz;
-          vz[(dh * BN * 128 + rows * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+        const int nz = (BN - rows) * (D / 64) * 8;  // 16-byte chunks to clear
+        for (int e = lane; e < nz; e += 32) {
+          const int chunk = e & 7, rd = e >> 3;
+          const int r = rows + rd / (D / 64), dh = rd % (D / 64);
+          *reinterpret_cast<uint4*>(sm.v[st] + tile_row_offset<D>(r, dh) + chunk * 16) = make_uint4(0, 0, 0, 0);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
       }
-      load_tile<D>(sm.v[st], &maps.v16, &maps.v1, &sm.v_full[st], a, b, kvh, kt, rows, lane);
+      load_tile<D>(sm.v[st], &maps.vb, &maps.v1, &sm.v_full[st], a, b, kvh, kt, rows, lane);
       issued = j + 1;
     }
     if (sm.abort && lane == 0) {
@@ -261,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kst = k_base + st * (BN * D * 2);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t bdesc = ptx::smem_desc(kst + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024, 2);
+          // K-major: 8-row atoms at stride GS, column half at +1024, 32 B per 16-column step.
+          const uint64_t bdesc = ptx::smem_desc(kst + (ks >> 2) * 1024 + (ks & 3) * 32, 16, (D / 64) * 1024, 2);
           ptx::mma_ts(tmem + S_COL[j & 1], tmem + Q_COL + ks * 8, bdesc, IDESC_QK, ks > 0);
         }
         ptx::mma_commit(&sm.s_full[j & 1]);
@@ -281,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vst = v_base + st * (BN * D * 2);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = ptx::smem_desc(vst + ks * 16 * 128, BN * 128, 1024, 2);
+          // MN-major: column halves at LBO = 1024, 8-row atoms at SBO = GS; one pool block per step.
+          const uint64_t bdesc = ptx::smem_desc(vst + ks * tile_row_offset<D>(16, 0), 1024, (D / 64) * 1024, 2);
           ptx::mma_ts(tmem + O_COL, tmem + S_COL[j & 1] + ks * 8, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         ptx::mma_commit(&sm.v_empty[st]);
@@ -332,14 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       float s[BN];
+      {
+        uint32_t r[BN / 32][32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + lane_base + S_COL[sb] + c * 32, r);
+        for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32(tmem + lane_base + S_COL[sb] + c * 32, r[c]);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+        for (int c = 0; c < BN / 32; ++c) {
+          ptx::reg_fence32(r[c]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
+        }
       }
-      ptx::tmem_wait_ld();
       const int j0 = (t_begin + j) * BN;
       const int nvis = lim - j0;
       if (nvis < BN) {
@@ -372,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             ptx::tmem_ld32(tmem + lane_base + O_COL + c * 32, r);
             ptx::tmem_wait_ld();
+            ptx::reg_fence32(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             ptx::tmem_st32(tmem + lane_base + O_COL + c * 32, r);
@@ -415,10 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
             ptx::tmem_ld32(tmem + lane_base + O_COL + c * 32, r);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence32(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(r[e]);
           }
-          ptx::tmem_wait_ld();
         } else {
           note_abort(sm, a.err);
           l = 0.f;
@@ -482,15 +504,32 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pool viewed as a 3-D tensor (D, Hkv, slots); box = 64 columns x 1 head x `rows` slots, 128-byte swizzle.
-bool encode_pool(CUtensorMap* m, const void* pool, int64_t num_slots, int Hkv, int D, bool bf16, int rows) {
+// Pool viewed as a 3-D tensor (D, Hkv, slots); box = 64 columns of one head in one slot, 128-byte swizzle.
+bool encode_pool_rows(CUtensorMap* m, const void* pool, int64_t num_slots, int Hkv, int D, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+  cuuint32_t box[3] = {64, 1, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Pool viewed as a 5-D tensor: (64 columns, 8 rows, D/64 column halves, slot groups of 8, Hkv heads),
+// strides (slot, 128 B, 8 slots, head).  Box = {64, 8, D/64, 2, 1} = one 16-row block of one head,
+// landing as [row group][column half][8 rows][128 B].
+bool encode_pool_blocks(CUtensorMap* m, const void* pool, int64_t num_slots, int Hkv, int D, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t slot = (cuuint64_t)Hkv * D * 2;
+  cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(num_slots / 8), (cuuint64_t)Hkv};
+  cuuint64_t strides[4] = {slot, 128, 8 * slot, (cuuint64_t)D * 2};
+  cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), 2, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
                   const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -500,10 +539,10 @@ template <int D, bool BF16>
 int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   TcMaps maps;
   const int64_t num_slots = a.num_blocks * 16;
-  if (!encode_pool(&maps.k16, a.k_pool, num_slots, a.Hkv, D, BF16, 16) ||
-      !encode_pool(&maps.v16, a.v_pool, num_slots, a.Hkv, D, BF16, 16) ||
-      !encode_pool(&maps.k1, a.k_pool, num_slots, a.Hkv, D, BF16, 1) ||
-      !encode_pool(&maps.v1, a.v_pool, num_slots, a.Hkv, D, BF16, 1))
+  if (!encode_pool_blocks(&maps.kb, a.k_pool, num_slots, a.Hkv, D, BF16) ||
+      !encode_pool_blocks(&maps.vb, a.v_pool, num_slots, a.Hkv, D, BF16) ||
+      !encode_pool_rows(&maps.k1, a.k_pool, num_slots, a.Hkv, D, BF16) ||
+      !encode_pool_rows(&maps.v1, a.v_pool, num_slots, a.Hkv, D, BF16))
     return (int)cudaErrorInvalidValue;
   // At least ~116 KB so that two CTAs never share an SM: each allocates all 512 TMEM columns.
   const size_t smem = sizeof(TcSmem<D>) + 1024 > (size_t)(116 * 1024) ? sizeof(TcSmem<D>) + 1024 : (size_t)(116 * 1024);

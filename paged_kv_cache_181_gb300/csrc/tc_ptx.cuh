@@ -82,8 +82,29 @@ PKV_DEVINLINE void tma_load_3d(void* dst, const void* tmap, int x, int y, int z,
       : "memory");
 }
 
+// 5-D tiled load global -> shared, completion counted in bytes on `bar`.
+PKV_DEVINLINE void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+      "%6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
 PKV_DEVINLINE void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async (16-byte, L2 only)
+
+// Copy 16 bytes global -> shared; with src_bytes == 0 nothing is read and the 16 bytes are zero-filled.
+PKV_DEVINLINE void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed (count not incremented).
+PKV_DEVINLINE void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -160,6 +181,17 @@ PKV_DEVINLINE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       "%16};" ::"r"(taddr),
       PKV_W8(0), PKV_W8(8)
       : "memory");
+}
+
+// Ties 32 registers to a point in the program: uses after this statement cannot be
+// hoisted above it (used right after tcgen05.wait::ld).
+PKV_DEVINLINE void reg_fence32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
 #undef PKV_R8
