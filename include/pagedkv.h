@@ -231,6 +231,41 @@ PKV_API pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const vo
                              size_t ws_bytes, uint32_t flags, void* stream);
 
 /*
+ * paged_attn_varlen_noalloc -- paged_attn_varlen for callers that cannot
+ * allocate GPU memory.  (The pages have no counterpart: this is a calling
+ * convention of this library.)
+ *
+ * Some callers may not call cudaMalloc or any allocating routine -- runtimes
+ * that give all device memory to their own arena at start-up, real-time loops
+ * where an allocation may synchronise the device or fail, plugin hosts that
+ * hand a kernel library no allocator -- yet long windows still want the
+ * key-range split, whose partial results need scratch space.  This call takes
+ * the same arguments as paged_attn_varlen minus the workspace and uses instead
+ * a fixed device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library's device code holds until the process exits.
+ * Nothing is allocated at call time.
+ *   - The array's device address is looked up once per device, inside the
+ *     first call made with that device current; make that first call before
+ *     any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (nothing
+ *     in it has to start at zero).  Calls whose GPU work overlaps -- other
+ *     streams, or unordered host threads -- race on it: do not issue them.
+ *   - Splits forced with PKV_SPLITS(n) that would need more than the array
+ *     holds (n * Tq * Hq * (D + 1) * 4 bytes) are refused with
+ *     PKV_ERR_CAPACITY before anything is launched; automatic planning never
+ *     asks for more than the array holds.
+ * Everything else (arguments, layouts, errors, results) is as for paged_attn_varlen.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+PKV_API pkv_status paged_attn_varlen_noalloc(const void* q, int64_t Tq, int Hq, const void* key_pool,
+                                             const void* value_pool, int64_t num_blocks, int block_size, int Hkv,
+                                             int D, pkv_dtype dt, const int32_t* block_table, int B, int W,
+                                             const int32_t* query_start_loc, const int32_t* seq_lens,
+                                             int max_query_len, int max_seq_len, float softmax_scale,
+                                             const pkv_segment* segs, const int32_t* seg_start, void* out,
+                                             uint32_t flags, void* stream);
+
+/*
  * pkv_check -- synchronise `stream`, read and clear the device error word
  * raised by kernels run with PKV_CHECK_BOUNDS on the current device.
  *   bits   host, out: PKV_DEVERR_* bits seen since the last pkv_check (may be NULL)

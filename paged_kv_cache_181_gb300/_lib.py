@@ -29,7 +29,7 @@ PKV_DEVERR_TIMEOUT = 32
 EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
     "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
-    "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches",
+    "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches", "paged_attn_varlen_noalloc",
 )
 
 
@@ -75,6 +75,9 @@ def _load() -> C.CDLL:
         "pkv_check": (C.c_int, [vp, C.POINTER(C.c_uint32)]),
         "pkv_sm_count": (C.c_int, []),
         "pkv_last_launches": (C.c_int, []),
+        "paged_attn_varlen_noalloc": (C.c_int, [vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int,
+                                                C.c_int, vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float, vp,
+                                                vp, vp, C.c_uint32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -223,6 +226,27 @@ def paged_attn_varlen(q, key_pool, value_pool, block_table, query_start_loc, seq
                               _dptr(seq_lens), int(max_query_len), int(max_seq_len), float(softmax_scale),
                               _dptr(segs), _dptr(seg_start), _dptr(out), _dptr(workspace), ws, flags,
                               _stream(stream)))
+    return out
+
+
+def paged_attn_varlen_noalloc(q, key_pool, value_pool, block_table, query_start_loc, seq_lens, max_query_len: int,
+                              max_seq_len: int, softmax_scale: float, *, segs=None, seg_start=None, out=None,
+                              flags: int = 0, block_size: int = 16, stream=None):
+    """paged_attn_varlen without a workspace: split partials go to the library's fixed scratch array.
+
+    For callers that cannot allocate device memory; see include/pagedkv.h.
+    """
+    torch = _torch()
+    Tq, hq, d = q.shape
+    hkv = key_pool.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    B, W = block_table.shape
+    _ok(lib.paged_attn_varlen_noalloc(_dptr(q), Tq, hq, _dptr(key_pool), _dptr(value_pool),
+                                      key_pool.shape[0] // block_size, block_size, hkv, d, dtype_code(q),
+                                      _dptr(block_table), B, W, _dptr(query_start_loc), _dptr(seq_lens),
+                                      int(max_query_len), int(max_seq_len), float(softmax_scale), _dptr(segs),
+                                      _dptr(seg_start), _dptr(out), flags, _stream(stream)))
     return out
 
 
