@@ -91,6 +91,58 @@ PKV_DEVINLINE void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int 
       : "memory");
 }
 
+// Multicast variants: the box lands at the same shared-memory offset in every CTA
+// of `mask` (within this cluster) and completes bytes on the same-offset mbarrier there.
+PKV_DEVINLINE void tma_load_5d_mc(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4, uint64_t* bar,
+                                  uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+PKV_DEVINLINE void tma_load_3d_mc(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+PKV_DEVINLINE uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release / acquire).
+PKV_DEVINLINE void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+PKV_DEVINLINE uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+PKV_DEVINLINE int ld_cluster_s32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in another CTA).
+PKV_DEVINLINE void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 PKV_DEVINLINE void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -148,6 +200,15 @@ PKV_DEVINLINE void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uin
 PKV_DEVINLINE void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// Same, arriving on the same-offset mbarrier in every CTA of `mask`.
+PKV_DEVINLINE void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 PKV_DEVINLINE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
