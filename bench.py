@@ -341,7 +341,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v2-blockbox"
+KERNEL_REV = "tc-v4-2q"
 
 
 def read_traffic(workload_name: str):

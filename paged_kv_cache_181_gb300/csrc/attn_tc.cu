@@ -7,32 +7,45 @@
 // of piecewise_attn.py expressed as a per-query key limit (every query sees a
 // prefix [0, limit) of its row's keys).
 //
-// One CTA = 128 queries of one (row, query head) and one key-range split.
-// Warp roles (192 threads):
-//   warp 0     producer: gathers 128-key K and V tiles through the block table
-//              with TMA, ONE box per 16-row pool block (4 KB for D=128): the
-//              pool is viewed as a 5-D tensor (64 columns, 8 rows, D/64
-//              column halves, row groups of 8, heads) so that a box lands as
-//              [block][row group][column half][8 rows][128 B], 128-byte
-//              swizzled.  Every 8-row x 128-byte atom then sits at a uniform
-//              stride (GS = D/64 KB) in both the key and the value tile, which
-//              is what the K-major (Q K^T) and MN-major (P V) shared-memory
-//              descriptors need.  (Two 2 KB boxes per block -- one per column
-//              half -- measured about half the load rate.)  3-stage ring per
-//              operand; a partly written last block is loaded row by row;
-//   warp 1     MMA issuer (one thread): S = Q K^T (Q from TMEM, K from shared
-//              memory) into one of two TMEM score buffers, then O += P V (P from
-//              TMEM, V from shared memory, MN-major) into the TMEM output;
-//   warps 2-5  softmax: one query row per thread, matching TMEM lane = row.
-//              Reads a score row from TMEM, masks, keeps a running maximum in
-//              the exp2 domain, writes bf16/f16 probabilities back into the
-//              score buffer's first columns for the P V MMA, and rescales its
-//              O row only when the maximum grows by more than 2^8 (otherwise
-//              the stale maximum is kept: probabilities stay <= 256).
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,256+D), Q after O.
-// Score buffers alternate, so QK^T of tile j+1 overlaps the softmax of tile j.
+// One CTA = 256 queries of one (row, query head) -- two 128-query tiles that
+// share every key/value tile -- and one key-range split.  Sharing halves the
+// key/value bytes each SM has to take in per FLOP, which is what bounds this
+// workload on this part (a one-tile CTA spent longer receiving its 64 KB per
+// key tile than its tensor core spent on the MMAs).
+//
+// Warp roles (384 threads = 3 warpgroups):
+//   warp 0     producer: TMA loads of both query tiles (once) and of the key
+//              and value tiles through the block table, ONE box per 16-row pool
+//              block: the pool is viewed as a 5-D tensor (64 columns, 8 rows,
+//              D/64 column halves, row groups of 8, heads), so a box lands as
+//              [row group][column half][8 rows][128 B], 128-byte swizzled, and
+//              every 8-row atom sits at a uniform stride in the tile (what the
+//              K-major and MN-major shared-memory descriptors need).  Key and
+//              value tiles share one ring of slots (K_j, V_j, K_j+1, ...); a
+//              partly written last block is loaded row by row; value rows past
+//              the last visible key are zeroed;
+//   warp 1     MMA issuer (one thread) and TMEM owner.  Per key tile j:
+//                P0.V_j -> O0, Q0.K_j+1 -> S0, P1.V_j -> O1, Q1.K_j+1 -> S1
+//              (A = Q from shared memory, or P from TMEM; B = K K-major or V
+//              MN-major from shared memory), so while one softmax group works
+//              on its scores the tensor core runs the other group's MMAs;
+//   warps 4-7  softmax of query tile 0, warps 8-11 of tile 1: one query row per
+//              thread (TMEM lane = row).  Reads a score row from TMEM, masks,
+//              keeps a running maximum in the exp2 domain, writes bf16/f16
+//              probabilities over the first half of the score columns, and
+//              rescales its O row only when the maximum grows by more than 2^8
+//              (otherwise the stale maximum is kept: probabilities stay <= 256).
+//              P.V of the previous tile is always complete by the time a score
+//              tile is ready (the score MMA was issued after it), so the rescale
+//              never waits.
+// Registers: the producer/MMA warpgroup (warps 0-3; 2 and 3 idle) gives up
+// registers to the two softmax warpgroups (setmaxnreg 104 / 200; the launch
+// provides 168 per thread and the host refuses to launch a build with another
+// count, so the split always adds up).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 after O0.
 // Every mbarrier wait is bounded in time (1 s); on expiry the CTA records
-// PKV_DEVERR_TIMEOUT, unwinds, waits for its own MMAs, frees TMEM and exits.
+// PKV_DEVERR_TIMEOUT, unwinds, waits for its own copies and MMAs, frees TMEM
+// and exits.
 
 #include <cuda.h>
 
@@ -42,34 +55,45 @@
 
 namespace {
 
-constexpr int BM = 128;      // queries per CTA
-constexpr int BN = 128;      // keys per tile
-constexpr int NST = 3;       // ring stages for K and for V
-constexpr int kThreads = 192;
+constexpr int BM = 128;  // queries per tile; two tiles per CTA
+constexpr int BN = 128;  // keys per tile
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;  // registers per thread the kernel is compiled to (checked at launch)
+constexpr int kRegsLow = 104;     // producer / MMA warpgroup
+constexpr int kRegsHigh = 200;    // softmax warpgroups: 128*104 + 256*200 == 384*168
+static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split must add up");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 template <int D>
+struct Cfg {
+  static constexpr int TILE = BN * D * 2;          // one key or value tile
+  static constexpr int NSLOT = D == 128 ? 5 : 10;  // ring slots (fits 227 KB with both query tiles)
+  static constexpr int GS = (D / 64) * 1024;       // stride of 8-row atoms in a key/value tile
+};
+
+template <int D>
 struct alignas(1024) TcSmem {
-  uint8_t k[NST][BN * D * 2];  // [D/64][BN rows][128 B], 128-byte swizzled
-  uint8_t v[NST][BN * D * 2];
-  uint64_t k_full[NST], k_empty[NST], v_full[NST], v_empty[NST];
-  uint64_t s_full[2], p_full[2], o_done, q_ready, mma_done;
+  uint8_t q[2][BM * D * 2];                 // [D/64][128 rows][128 B] per query tile, 128-byte swizzled
+  uint8_t kv[Cfg<D>::NSLOT][Cfg<D>::TILE];  // [block][row group][column half][8 rows][128 B]
+  uint64_t full[Cfg<D>::NSLOT], empty[Cfg<D>::NSLOT];
+  uint64_t q_full, s_full[2], p_full[2], mma_done;
   uint32_t tmem_base;
   int lim_max;
   int abort;
 };
 
 struct TcMaps {
-  CUtensorMap kb, vb;  // 5-D views, box = one whole pool block of one head
-  CUtensorMap k1, v1;  // 3-D views (D, Hkv, slots), box = 64 columns of one row (partial blocks)
+  CUtensorMap q;       // (D, Hq, Tq), box = 64 columns x 128 tokens of one head
+  CUtensorMap kb, vb;  // 5-D pool views, box = one whole 16-row pool block of one head
+  CUtensorMap k1, v1;  // 3-D pool views (D, Hkv, slots), box = 64 columns of one row (partial blocks)
 };
 
-// Tile layout: byte offset of 128-byte row (tile row r, column half dh).
+// Byte offset of 128-byte row (tile row r, column half dh) in a key/value tile.
 template <int D>
 __host__ __device__ constexpr int tile_row_offset(int r, int dh) {
-  return (r >> 4) * (2 * (D / 64) * 1024) + ((r >> 3) & 1) * ((D / 64) * 1024) + dh * 1024 + (r & 7) * 128;
+  return (r >> 4) * (2 * Cfg<D>::GS) + ((r >> 3) & 1) * Cfg<D>::GS + dh * 1024 + (r & 7) * 128;
 }
 
 template <int D>
@@ -85,7 +109,7 @@ PKV_DEVINLINE bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Producer: gather key rows [j0, j0 + rows) of one (row, kv head) into a stage.
+// Producer: gather key rows [kt*BN, kt*BN + rows) of one (row, kv head) into a slot.
 template <int D>
 PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensorMap* m1, uint64_t* full,
                              const PkvAttnArgs& a, int b, int kvh, int kt, int rows, int lane) {
@@ -100,8 +124,7 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensor
       pkv_raise(a.err, PKV_DEVERR_BLOCK);
       blk = 0;
     }
-    const bool partial = (p == n_pages - 1) && rem != 0;
-    if (!partial) {
+    if (!(p == n_pages - 1 && rem != 0)) {
       ptx::tma_load_5d(dst + tile_row_offset<D>(p * 16, 0), mb, 0, 0, 0, blk * 2, kvh, full);
     } else {
       for (int r = 0; r < rem; ++r)
@@ -115,17 +138,18 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensor
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcMaps maps, const PkvAttnArgs a) {
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = a.Hq / a.Hkv;
-  const int n_qt = (a.max_query_len + BM - 1) / BM;
+  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
   int u = blockIdx.x;
   const int gi = u % g;
   u /= g;
-  const int qt = u % n_qt;
-  u /= n_qt;
+  const int qp = u % n_qp;
+  u /= n_qp;
   const int kvh = u % a.Hkv;
   const int b = u / a.Hkv;
   const int h = kvh * g + gi;
@@ -136,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int L = a.seq_lens[b];
   if (a.check) {
     const int lmax = a.W * 16 < a.max_seq_len ? a.W * 16 : a.max_seq_len;
-    const bool first = tid == 0 && qt == 0 && gi == 0 && split == 0;
+    const bool first = tid == 0 && qp == 0 && gi == 0 && split == 0;
     if (Sq < 0 || Sq > a.max_query_len) {
       if (first) pkv_raise(a.err, PKV_DEVERR_QUERY);
       Sq = Sq < 0 ? 0 : a.max_query_len;
@@ -146,26 +170,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       L = L > lmax ? lmax : (L < 0 ? 0 : L);
     }
   }
-  const int i0 = qt * BM;
+  const int i0 = qp * 2 * BM;
   if (i0 >= Sq) return;  // whole CTA: no query rows here
   // A pipeline timeout earlier in this launch (or an unchecked earlier one) means
   // results are already invalid: fail fast instead of waiting again.
   if (*(volatile unsigned int*)a.err & PKV_DEVERR_TIMEOUT) return;
+  const int n_q = i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
 
-  // ---------------------------------------------------------------- setup
+  // ---------------------------------------------------------------- set-up
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) {
-      ptx::mbar_init(&sm.k_full[s], 1);
-      ptx::mbar_init(&sm.k_empty[s], 1);
-      ptx::mbar_init(&sm.v_full[s], 1);
-      ptx::mbar_init(&sm.v_empty[s], 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(&sm.full[s], 1);
+      ptx::mbar_init(&sm.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&sm.s_full[s], 1);
-      ptx::mbar_init(&sm.p_full[s], 128);
+    ptx::mbar_init(&sm.q_full, 1);
+    for (int w = 0; w < 2; ++w) {
+      ptx::mbar_init(&sm.s_full[w], 1);
+      ptx::mbar_init(&sm.p_full[w], 128);
     }
-    ptx::mbar_init(&sm.o_done, 1);
-    ptx::mbar_init(&sm.q_ready, 128);
     ptx::mbar_init(&sm.mma_done, 1);
     sm.lim_max = 0;
     sm.abort = 0;
@@ -181,24 +203,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // Per-row key limit (softmax threads own rows).
+  // Softmax groups: warps 4-7 own query tile 0, warps 8-11 tile 1; TMEM lane quarter = warp % 4.
+  const int grp = warp >= 8 ? 1 : 0;
+  const bool is_softmax = warp >= 4;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
+  const int i = i0 + grp * BM + row;  // local query index of this thread's row
   int lim = 0;
-  if (warp >= 2) {
-    const int i = i0 + row;
-    if (i < Sq) {
-      bool uncovered = false;
-      int s_begin = 0, s_end = 0;
-      if (a.segs) {
-        s_begin = a.seg_start[b];
-        s_end = a.seg_start[b + 1];
-      }
-      lim = pkv_row_limit(L - Sq + i, L, a.segs, s_begin, s_end, &uncovered);
-      if (a.check && uncovered) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
+  if (is_softmax && i < Sq) {
+    bool uncovered = false;
+    int s_begin = 0, s_end = 0;
+    if (a.segs) {
+      s_begin = a.seg_start[b];
+      s_end = a.seg_start[b + 1];
     }
-    atomicMax(&sm.lim_max, lim);
+    lim = pkv_row_limit(L - Sq + i, L, a.segs, s_begin, s_end, &uncovered);
+    if (a.check && uncovered) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
   }
+  if (is_softmax) atomicMax(&sm.lim_max, lim);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -211,98 +233,119 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = min(n_tiles, t_begin + per);
   const int n = t_end > t_begin ? t_end - t_begin : 0;
 
-  constexpr uint32_t S_COL[2] = {0, 128};
-  constexpr uint32_t O_COL = 256;
-  constexpr uint32_t Q_COL = 256 + D;
+  constexpr uint32_t O_COL[2] = {256, 256 + D};
   constexpr uint32_t IDESC_QK = ptx::idesc_f16(BM, BN, BF16 ? 1 : 0, 0);
   constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16 ? 1 : 0, 1);
 
+  if (warp < 4) {
+  ptx::regs_dec<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
-    for (int j = 0; j < n; ++j) {
+    if (n > 0) {
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(n_q * BM * D * 2));
+        for (int t = 0; t < n_q; ++t)
+#pragma unroll
+          for (int dh = 0; dh < D / 64; ++dh)  // rows past the last token read as zeros
+            ptx::tma_load_3d(sm.q[t] + dh * (BM * 128), &maps.q, dh * 64, h, q0 + i0 + t * BM, &sm.q_full);
+      }
+      __syncwarp();
+    }
+    for (int idx = 0; idx < 2 * n; ++idx) {
       if (__any_sync(0xffffffffu, sm.abort != 0)) break;
-      const int st = j % NST, use = j / NST;
-      const int kt = t_begin + j;
-      const int j0 = kt * BN;
-      const int rows = min(BN, kv_hi - j0);
-      if (j >= NST && !warp_wait(&sm.k_empty[st], (use - 1) & 1, &sm.abort, lane)) {
+      const int pos = idx % C::NSLOT, use = idx / C::NSLOT;
+      const bool is_v = idx & 1;
+      const int kt = t_begin + (idx >> 1);
+      const int rows = min(BN, kv_hi - kt * BN);
+      if (idx >= C::NSLOT && !warp_wait(&sm.empty[pos], (use - 1) & 1, &sm.abort, lane)) {
         if (lane == 0) note_abort(sm, a.err);
         break;
       }
-      load_tile<D>(sm.k[st], &maps.kb, &maps.k1, &sm.k_full[st], a, b, kvh, kt, rows, lane);
-      if (j >= NST && !warp_wait(&sm.v_empty[st], (use - 1) & 1, &sm.abort, lane)) {
-        if (lane == 0) note_abort(sm, a.err);
-        issued = j;  // K of tile j is in flight
-        break;
-      }
-      if (rows < BN) {
-        // Key rows past the last visible key are never loaded: zero them in V
-        // (P is 0 there, but 0 * NaN would not be).  Zeroing whole 128-byte
-        // rows is independent of the swizzle.
+      if (is_v && rows < BN) {
+        // Value rows past the last visible key are never loaded: zero them (P is 0 there,
+        // but 0 * NaN would not be).  Whole 128-byte rows: independent of the swizzle.
         const int nz = (BN - rows) * (D / 64) * 8;  // 16-byte chunks to clear
         for (int e = lane; e < nz; e += 32) {
           const int chunk = e & 7, rd = e >> 3;
           const int r = rows + rd / (D / 64), dh = rd % (D / 64);
-          *reinterpret_cast<uint4*>(sm.v[st] + tile_row_offset<D>(r, dh) + chunk * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sm.kv[pos] + tile_row_offset<D>(r, dh) + chunk * 16) = make_uint4(0, 0, 0, 0);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
       }
-      load_tile<D>(sm.v[st], &maps.vb, &maps.v1, &sm.v_full[st], a, b, kvh, kt, rows, lane);
-      issued = j + 1;
+      if (is_v)
+        load_tile<D>(sm.kv[pos], &maps.vb, &maps.v1, &sm.full[pos], a, b, kvh, kt, rows, lane);
+      else
+        load_tile<D>(sm.kv[pos], &maps.kb, &maps.k1, &sm.full[pos], a, b, kvh, kt, rows, lane);
     }
     if (sm.abort && lane == 0) {
-      // Let the copies already issued land before the shared memory goes away.
-      for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
-        const int st = j % NST, use = j / NST;
-        int dummy = 0;
-        ptx::mbar_wait(&sm.k_full[st], use & 1, &dummy, kWaitLimitNs);
-        ptx::mbar_wait(&sm.v_full[st], use & 1, &dummy, kWaitLimitNs);
-      }
+      // Let copies already issued land before the shared memory goes away.
+      int dummy = 0;
+      ptx::mbar_wait(&sm.q_full, 0, &dummy, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      const uint32_t k_base = ptx::smem_u32(sm.k[0]);
-      const uint32_t v_base = ptx::smem_u32(sm.v[0]);
-      bool ok = ptx::mbar_wait(&sm.q_ready, 0, &sm.abort, kWaitLimitNs);
+      const uint32_t q_base[2] = {ptx::smem_u32(sm.q[0]), ptx::smem_u32(sm.q[1])};
+      const uint32_t kv_base = ptx::smem_u32(sm.kv[0]);
+      bool ok = ptx::mbar_wait(&sm.q_full, 0, &sm.abort, kWaitLimitNs);
       ptx::tc_fence_after();
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % NST;
-        if (!ptx::mbar_wait(&sm.k_full[st], (j / NST) & 1, &sm.abort, kWaitLimitNs)) return false;
+      auto slot_ready = [&](int idx) -> bool {
+        const int pos = idx % C::NSLOT;
+        if (!ptx::mbar_wait(&sm.full[pos], (idx / C::NSLOT) & 1, &sm.abort, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        const uint32_t kst = k_base + st * (BN * D * 2);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // K-major: 8-row atoms at stride GS, column half at +1024, 32 B per 16-column step.
-          const uint64_t bdesc = ptx::smem_desc(kst + (ks >> 2) * 1024 + (ks & 3) * 32, 16, (D / 64) * 1024, 2);
-          ptx::mma_ts(tmem + S_COL[j & 1], tmem + Q_COL + ks * 8, bdesc, IDESC_QK, ks > 0);
-        }
-        ptx::mma_commit(&sm.s_full[j & 1]);
-        ptx::mma_commit(&sm.k_empty[st]);
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      if (ok && n > 1) ok = issue_qk(1);
+      // S_w = Q_w K_j^T (key tile j sits in slot (2j) % NSLOT)
+      auto qk = [&](int w, int j) {
+        const uint32_t kst = kv_base + ((2 * j) % C::NSLOT) * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          // Q: [half][128 rows][128 B] -> 8-row atoms at 1024 B, column half at BM*128 B
+          const uint64_t adesc = ptx::smem_desc(q_base[w] + (ks >> 2) * (BM * 128) + (ks & 3) * 32, 16, 1024, 2);
+          // K: block-interleaved -> 8-row atoms at GS, column half at +1024 B
+          const uint64_t bdesc = ptx::smem_desc(kst + (ks >> 2) * 1024 + (ks & 3) * 32, 16, C::GS, 2);
+          ptx::mma_ss(tmem + 128 * w, adesc, bdesc, IDESC_QK, ks > 0);
+        }
+        ptx::mma_commit(&sm.s_full[w]);
+      };
+      // O_w (+)= P_w V_j (value tile j sits in slot (2j+1) % NSLOT; P_w over the first columns of S_w)
+      auto pv = [&](int w, int j) {
+        const uint32_t vst = kv_base + ((2 * j + 1) % C::NSLOT) * C::TILE;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t bdesc = ptx::smem_desc(vst + ks * (2 * C::GS), 1024, C::GS, 2);
+          ptx::mma_ts(tmem + O_COL[w], tmem + 128 * w + ks * 8, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = slot_ready(0);
+      if (ok) {
+        for (int w = 0; w < n_q; ++w) qk(w, 0);
+        ptx::mma_commit(&sm.empty[0]);  // key tile 0 consumed
+      }
       for (int j = 0; ok && j < n; ++j) {
-        const int st = j % NST;
-        if (!ptx::mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, &sm.abort, kWaitLimitNs) ||
-            !ptx::mbar_wait(&sm.v_full[st], (j / NST) & 1, &sm.abort, kWaitLimitNs)) {
+        const bool next = j + 1 < n;
+        if (!slot_ready(2 * j + 1)) {  // value tile j
           ok = false;
           break;
         }
-        ptx::tc_fence_after();
-        const uint32_t vst = v_base + st * (BN * D * 2);
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          // MN-major: column halves at LBO = 1024, 8-row atoms at SBO = GS; one pool block per step.
-          const uint64_t bdesc = ptx::smem_desc(vst + ks * tile_row_offset<D>(16, 0), 1024, (D / 64) * 1024, 2);
-          ptx::mma_ts(tmem + O_COL, tmem + S_COL[j & 1] + ks * 8, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+        for (int w = 0; w < n_q && ok; ++w) {
+          if (!ptx::mbar_wait(&sm.p_full[w], j & 1, &sm.abort, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          pv(w, j);
+          if (w == n_q - 1) ptx::mma_commit(&sm.empty[(2 * j + 1) % C::NSLOT]);  // value tile j consumed
+          if (next) {
+            if (w == 0 && !slot_ready(2 * j + 2)) {  // key tile j+1
+              ok = false;
+              break;
+            }
+            qk(w, j + 1);
+            if (w == n_q - 1) ptx::mma_commit(&sm.empty[(2 * j + 2) % C::NSLOT]);  // key tile j+1 consumed
+          }
         }
-        ptx::mma_commit(&sm.v_empty[st]);
-        ptx::mma_commit(&sm.o_done);
-        if (j + 2 < n) ok = issue_qk(j + 2);
       }
       if (!ok) note_abort(sm, a.err);
       // Everything issued must finish before TMEM is released.
@@ -310,39 +353,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dummy = 0;
       ptx::mbar_wait(&sm.mma_done, 0, &dummy, kWaitLimitNs);
     }
+  }
   } else {
-    // ------------------------------------------------------------ softmax rows
+  ptx::regs_inc<kRegsHigh>();
+  if (grp < n_q) {
+    // ------------------------------------------------------------ softmax rows of query tile grp
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int i = i0 + row;
+    const uint32_t S_COL = 128 * grp;
     const bool valid = i < Sq;
     const int64_t tok = (int64_t)q0 + i;
-    // Q row -> TMEM (packed pairs of 16-bit values, column c holds elements 2c and 2c+1).
-    {
-      const uint4* src = reinterpret_cast<const uint4*>((const uint16_t*)a.q + (tok * a.Hq + h) * D);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t r[32];
-#pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
-          const uint4 x = valid ? src[c * 8 + v4] : make_uint4(0, 0, 0, 0);
-          r[v4 * 4 + 0] = x.x;
-          r[v4 * 4 + 1] = x.y;
-          r[v4 * 4 + 2] = x.z;
-          r[v4 * 4 + 3] = x.w;
-        }
-        ptx::tmem_st32(tmem + lane_base + Q_COL + c * 32, r);
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.q_ready);
-    }
     const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm.s_full[sb], (j >> 1) & 1, &sm.abort, kWaitLimitNs))) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm.s_full[grp], j & 1, &sm.abort, kWaitLimitNs))) {
         ok = false;
         break;
       }
@@ -351,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t r[BN / 32][32];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32(tmem + lane_base + S_COL[sb] + c * 32, r[c]);
+        for (int c = 0; c < BN / 32; ++c) ptx::tmem_ld32(tmem + lane_base + S_COL + c * 32, r[c]);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
@@ -376,26 +401,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       // TMEM loads/stores are warp-collective: the warp rescales together when any
-      // of its rows needs it (alpha = 1 for the others).
+      // of its rows needs it (alpha = 1 for the others).  P.V of tile j-1 is complete:
+      // the score MMA of tile j, whose completion was just observed, was issued after it.
       const bool need = m_tile > m_ref + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ptx::ex2(m_ref - m_tile) : 1.f;  // 0 on a row's first visible tile
         l *= alpha;
         if (j > 0) {
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&sm.o_done, (j - 1) & 1, &sm.abort, kWaitLimitNs))) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            ptx::tmem_ld32(tmem + lane_base + O_COL + c * 32, r);
+            ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r);
             ptx::tmem_wait_ld();
             ptx::reg_fence32(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            ptx::tmem_st32(tmem + lane_base + O_COL + c * 32, r);
+            ptx::tmem_st32(tmem + lane_base + O_COL[grp] + c * 32, r);
           }
         }
         if (need) m_ref = m_tile;
@@ -414,12 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           l1 += p1;
           r[e] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
         }
-        ptx::tmem_st16(tmem + lane_base + S_COL[sb] + c * 16, r);
+        ptx::tmem_st16(tmem + lane_base + S_COL + c * 16, r);
       }
       l += l0 + l1;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.p_full[sb]);
+      ptx::mbar_arrive(&sm.p_full[grp]);
     }
     if (!ok) note_abort(sm, a.err);
 
@@ -427,15 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       float o[D];
       if (n > 0) {
-        // Not o_done: when the last tile is reached that barrier can still be two
-        // phases behind (P.V of tile n-2 in flight), and a parity wait would then
-        // pass at once.  mma_done completes exactly once, after every MMA.
+        // mma_done completes exactly once, after every MMA of the CTA.
         if (__all_sync(0xffffffffu, ptx::mbar_wait(&sm.mma_done, 0, &sm.abort, kWaitLimitNs))) {
           ptx::tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            ptx::tmem_ld32(tmem + lane_base + O_COL + c * 32, r);
+            ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r);
             ptx::tmem_wait_ld();
             ptx::reg_fence32(r);
 #pragma unroll
@@ -476,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  }  // softmax warpgroups
+
   // ---------------------------------------------------------------- teardown
   ptx::tc_fence_before();
   __syncthreads();
@@ -504,61 +525,55 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pool viewed as a 3-D tensor (D, Hkv, slots); box = 64 columns of one head in one slot, 128-byte swizzle.
-bool encode_pool_rows(CUtensorMap* m, const void* pool, int64_t num_slots, int Hkv, int D, bool bf16) {
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-  cuuint32_t box[3] = {64, 1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                  const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Pool viewed as a 5-D tensor: (64 columns, 8 rows, D/64 column halves, slot groups of 8, Hkv heads),
-// strides (slot, 128 B, 8 slots, head).  Box = {64, 8, D/64, 2, 1} = one 16-row block of one head,
-// landing as [row group][column half][8 rows][128 B].
-bool encode_pool_blocks(CUtensorMap* m, const void* pool, int64_t num_slots, int Hkv, int D, bool bf16) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t slot = (cuuint64_t)Hkv * D * 2;
-  cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(num_slots / 8), (cuuint64_t)Hkv};
-  cuuint64_t strides[4] = {slot, 128, 8 * slot, (cuuint64_t)D * 2};
-  cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), 2, 1};
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
-                  const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool BF16>
 int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   TcMaps maps;
   const int64_t num_slots = a.num_blocks * 16;
-  if (!encode_pool_blocks(&maps.kb, a.k_pool, num_slots, a.Hkv, D, BF16) ||
-      !encode_pool_blocks(&maps.vb, a.v_pool, num_slots, a.Hkv, D, BF16) ||
-      !encode_pool_rows(&maps.k1, a.k_pool, num_slots, a.Hkv, D, BF16) ||
-      !encode_pool_rows(&maps.v1, a.v_pool, num_slots, a.Hkv, D, BF16))
+  const cuuint64_t slot = (cuuint64_t)a.Hkv * D * 2;
+  // Pool as 5-D: (64 columns, 8 rows, D/64 column halves, slot groups of 8, heads),
+  // strides (slot, 128 B, 8 slots, head); box = one 16-row block of one head.
+  const cuuint64_t dims5[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(num_slots / 8), (cuuint64_t)a.Hkv};
+  const cuuint64_t str5[4] = {slot, 128, 8 * slot, (cuuint64_t)D * 2};
+  const cuuint32_t box5[5] = {64, 8, (cuuint32_t)(D / 64), 2, 1};
+  const cuuint64_t dims3[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)num_slots};
+  const cuuint64_t str3[2] = {(cuuint64_t)D * 2, slot};
+  const cuuint32_t box1[3] = {64, 1, 1};
+  const cuuint64_t dimsq[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.Tq};
+  const cuuint64_t strq[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+  const cuuint32_t boxq[3] = {64, 1, BM};
+  if (!encode(&maps.kb, a.k_pool, 5, dims5, str5, box5, BF16) || !encode(&maps.vb, a.v_pool, 5, dims5, str5, box5, BF16) ||
+      !encode(&maps.k1, a.k_pool, 3, dims3, str3, box1, BF16) || !encode(&maps.v1, a.v_pool, 3, dims3, str3, box1, BF16) ||
+      !encode(&maps.q, a.q, 3, dimsq, strq, boxq, BF16))
     return (int)cudaErrorInvalidValue;
-  // At least ~116 KB so that two CTAs never share an SM: each allocates all 512 TMEM columns.
-  const size_t smem = sizeof(TcSmem<D>) + 1024 > (size_t)(116 * 1024) ? sizeof(TcSmem<D>) + 1024 : (size_t)(116 * 1024);
+  const size_t smem = sizeof(TcSmem<D>) + 1024;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The warpgroup register split is only valid for the register count it was sized for.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, BF16>);
+    if (e != cudaSuccess) return (int)e;
+    if (fa.numRegs != kLaunchRegs) return (int)cudaErrorInvalidKernelImage;
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     attr_set[dev] = true;
   }
   const int g = a.Hq / a.Hkv;
-  const int n_qt = (a.max_query_len + BM - 1) / BM;
-  const int64_t units = (int64_t)a.B * a.Hkv * n_qt * g;
-  if (units > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)units, (unsigned)a.num_splits);
+  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
+  const int64_t ctas = (int64_t)a.B * a.Hkv * n_qp * g;
+  if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)ctas, (unsigned)a.num_splits);
   attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a);
   return (int)cudaGetLastError();
 }
@@ -569,6 +584,7 @@ bool pkv_attn_tc_supports(pkv_dtype dt, int D) { return (dt == PKV_BF16 || dt ==
 
 int pkv_launch_attn_tc(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
   if (!pkv_attn_tc_supports(dt, a.D) || !(a.scale > 0.f) || !a.err) return -1;
+  if (a.Tq > 0x7fffffff) return -1;
   cudaStream_t s = (cudaStream_t)stream;
   if (a.D == 128) return dt == PKV_BF16 ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
   return dt == PKV_BF16 ? launch_tc<64, true>(a, s) : launch_tc<64, false>(a, s);

@@ -172,6 +172,40 @@ PKV_DEVINLINE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// ---- CTA-pair (cta_group::2) forms: every tcgen05 instruction of a kernel uses one cta_group.
+// Allocation and deallocation are performed collectively by one warp in each CTA of the pair.
+PKV_DEVINLINE void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+PKV_DEVINLINE void tmem_relinquish2() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory"); }
+PKV_DEVINLINE void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Pair MMA issued by one thread of the even CTA: M = 256 rows, rows 0-127 (A and D) in the even
+// CTA's TMEM and rows 128-255 in the odd CTA's, at the same addresses; B's N columns split in
+// halves, each held at the same shared-memory offset in one CTA.
+PKV_DEVINLINE void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the same-offset mbarrier of every CTA in `mask` once the pair MMAs issued so far are done.
+PKV_DEVINLINE void mma_commit2_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]   (kind::f16, fp32 accumulate)
 PKV_DEVINLINE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -257,6 +291,18 @@ PKV_DEVINLINE void reg_fence32(uint32_t (&r)[32]) {
 
 #undef PKV_R8
 #undef PKV_W8
+
+// ---------------------------------------------------------------- register budget
+
+// Per-warpgroup register budget (all warps of the warpgroup execute the same one).
+template <uint32_t N>
+PKV_DEVINLINE void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+PKV_DEVINLINE void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---------------------------------------------------------------- descriptors
 
