@@ -326,6 +326,9 @@ def run_ours(args, world, rank, local):
 
     traffic = read_traffic(w.name)
 
+    # Paged vs contiguous K/V on the same data (the pages' gather-then-attend path).
+    kv_layout = measure_kv_layout(case, stream, attn_avg, row_bytes) if not args.no_kv_layout else None
+
     # e2e: inputs from pinned host memory every step, outputs back to the host.
     e2e = run_e2e(case, args, world, stream) if not args.no_e2e else None
 
@@ -348,13 +351,67 @@ def run_ours(args, world, rank, local):
     }
     if e2e is not None:
         result["e2e"] = e2e
+    if kv_layout is not None:
+        result["kv_layout"] = kv_layout
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = {k: v for k, v in cpu_oracle_sample(w).items() if k != "seconds"}
     if rank == 0:
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v4-2q"
+KERNEL_REV = "tc-v5-contig"
+
+
+def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
+    """Per layer: the block gather of the visible window into staging buffers, the same attention on the
+    staged (contiguous) K/V, and the re-gather of the current chunk's blocks only (history kept staged)."""
+    import torch
+
+    layers = case.layers
+    st = case.make_staging()
+    for l in range(min(3, layers)):
+        case.stage(l, st, stream=stream)
+        case.attend_contiguous(l, st, stream=stream)
+    torch.cuda.synchronize()
+
+    def burst(fn, reps=3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        out = []
+        for _ in range(reps):
+            e0.record(stream)
+            for l in range(layers):
+                fn(l)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) / layers)
+        return statistics.median(out)
+
+    gather_ms = burst(lambda l: case.stage(l, st, stream=stream))
+    regather_ms = burst(lambda l: case.stage(l, st, reuse_history=True, stream=stream))
+    # Attention on staged K/V: events around each launch, every layer staged just before.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    contig_ms = []
+    for _ in range(2):
+        for l in range(layers):
+            case.stage(l, st, stream=stream)
+            ev[l][0].record(stream)
+            case.attend_contiguous(l, st, stream=stream)
+            ev[l][1].record(stream)
+        torch.cuda.synchronize()
+        contig_ms += [ev[l][0].elapsed_time(ev[l][1]) for l in range(layers)]
+    contig = statistics.mean(contig_ms)
+    staged_rows = case.w.batch * st.used_blocks * case.w.block_size
+    chunk_rows = case.w.batch * (st.used_blocks - st.first_block) * case.w.block_size
+    res = {
+        "paged_attn_ms": paged_ms, "contiguous_attn_ms": contig, "paged_over_contiguous": paged_ms / contig,
+        "gather_ms": gather_ms, "gather_gbs": staged_rows * row_bytes * 4 / (gather_ms * 1e-3) / 1e9,
+        "regather_chunk_ms": regather_ms, "regather_blocks_per_row": st.used_blocks - st.first_block,
+        "gather_then_attend_ms": gather_ms + contig, "regather_then_attend_ms": regather_ms + contig,
+        "chunk_rows": chunk_rows,
+    }
+    del st
+    torch.cuda.empty_cache()
+    return res
 
 
 def read_traffic(workload_name: str):
@@ -465,6 +522,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kv-layout", action="store_true", help="skip the paged vs contiguous K/V comparison")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -69,6 +69,11 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 #define PKV_CHECK_BOUNDS 0x1u  /* validate device metadata in the kernels */
 #define PKV_FORCE_SIMT 0x2u    /* attention: use the CUDA-core kernel even for bf16/f16 */
 #define PKV_NO_SPLIT 0x4u      /* attention: never split the key range */
+/* attention: every row's block-table entries are consecutive (entry i = entry 0 + i), e.g. K/V staged by
+ * paged_kv_gather; the tensor-core kernel then loads a whole 128-key tile per TMA box instead of one box per
+ * 16-token block.  With PKV_CHECK_BOUNDS a row that breaks the promise is flagged (PKV_DEVERR_BLOCK) and
+ * loaded block by block. */
+#define PKV_CONTIGUOUS_KV 0x8u
 /* attention: force n (1..8) key-range splits (needs workspace); 0 = plan automatically */
 #define PKV_SPLITS(n) ((((uint32_t)(n)) & 0xffu) << 8)
 
@@ -192,6 +197,23 @@ PKV_API pkv_status pkv_block_table_row(const int32_t* video_blocks, int64_t n_vi
 PKV_API pkv_status paged_kv_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t T, void* key_pool,
                           void* value_pool, int64_t num_slots, int Hkv, int D, pkv_dtype dt, uint32_t flags,
                           void* stream);
+
+/*
+ * paged_kv_gather -- copy blocks [first_block, first_block + n_blocks) of every row's block table into
+ * contiguous staging buffers: stage[b][first_block*16 + t] = pool[table[b*W + first_block + t/16]*16 + t%16]
+ * for t < n_blocks*16, for K and V (paged_attention.py, _stage_window / the contiguous gather branch of
+ * ar_diffusion_paged_attention; first_block > 0 re-gathers only the current chunk's blocks when the
+ * history is already staged, as stage_first_block does there).  A bit copy; one launch for K and V.
+ *   key_pool, value_pool  device [num_blocks*16, Hkv, D]
+ *   block_table           device [B, W] int32
+ *   stage_k, stage_v      device [B, stage_rows, Hkv, D]; needs (first_block + n_blocks) * 16 <= stage_rows
+ * Errors: PKV_ERR_INVALID_ARG (sizes, alignment, first_block + n_blocks > W); with PKV_CHECK_BOUNDS block
+ * ids outside [0, num_blocks) are flagged (PKV_DEVERR_BLOCK) and their rows not copied.
+ */
+PKV_API pkv_status paged_kv_gather(const void* key_pool, const void* value_pool, int64_t num_blocks,
+                                   const int32_t* block_table, int B, int W, int first_block, int n_blocks,
+                                   void* stage_k, void* stage_v, int64_t stage_rows, int Hkv, int D, pkv_dtype dt,
+                                   uint32_t flags, void* stream);
 
 /*
  * paged_attn_workspace_size -- bytes of workspace paged_attn_varlen may use

@@ -22,6 +22,7 @@ PKV_F32, PKV_BF16, PKV_F16 = 0, 1, 2
 PKV_CHECK_BOUNDS = 0x1
 PKV_FORCE_SIMT = 0x2
 PKV_NO_SPLIT = 0x4
+PKV_CONTIGUOUS_KV = 0x8
 PKV_SEG_CAUSAL, PKV_SEG_FULL = 0, 1
 PKV_DEVERR_SLOT, PKV_DEVERR_BLOCK, PKV_DEVERR_SEQLEN, PKV_DEVERR_QUERY, PKV_DEVERR_SEGMENT = 1, 2, 4, 8, 16
 PKV_DEVERR_TIMEOUT = 32
@@ -30,6 +31,7 @@ EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
     "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
     "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches", "paged_attn_varlen_noalloc",
+    "paged_kv_gather",
 )
 
 
@@ -68,6 +70,8 @@ def _load() -> C.CDLL:
                                           i64p]),
         "paged_kv_write": (C.c_int, [vp, vp, vp, C.c_int64, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_uint32,
                                      vp]),
+        "paged_kv_gather": (C.c_int, [vp, vp, C.c_int64, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, C.c_int64,
+                                      C.c_int, C.c_int, C.c_int, C.c_uint32, vp]),
         "paged_attn_workspace_size": (C.c_size_t, [C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
         "paged_attn_varlen": (C.c_int, [vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int,
                                         vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp,
@@ -196,6 +200,28 @@ def paged_kv_write(k, v, slot_mapping, key_pool, value_pool, *, flags: int = 0, 
         raise ValueError("paged_kv_write: slot_mapping must be int64 [T]")
     _ok(lib.paged_kv_write(_dptr(k), _dptr(v), _dptr(slot_mapping), T, _dptr(key_pool), _dptr(value_pool),
                            key_pool.shape[0], hkv, d, dtype_code(k), flags, _stream(stream)))
+
+
+def paged_kv_gather(key_pool, value_pool, block_table, stage_k, stage_v, *, first_block: int = 0,
+                    n_blocks: int | None = None, flags: int = 0, block_size: int = 16, stream=None) -> None:
+    """Copy table blocks [first_block, first_block + n_blocks) of every row into ``stage_k/v [B, rows, Hkv, D]``."""
+    torch = _torch()
+    B, W = block_table.shape
+    if n_blocks is None:
+        n_blocks = W - first_block
+    for t in (key_pool, value_pool, block_table, stage_k, stage_v):
+        if not t.is_contiguous():
+            raise ValueError("paged_kv_gather: tensors must be contiguous")
+    if block_table.dtype != torch.int32:
+        raise ValueError("paged_kv_gather: block_table must be int32")
+    if stage_k.shape != stage_v.shape or stage_k.shape[0] != B or stage_k.shape[2:] != key_pool.shape[1:]:
+        raise ValueError("paged_kv_gather: staging buffers must be [B, rows, Hkv, D]")
+    if len({key_pool.dtype, value_pool.dtype, stage_k.dtype, stage_v.dtype}) != 1:
+        raise ValueError("paged_kv_gather: pools and staging buffers must share one dtype")
+    hkv, d = key_pool.shape[1:]
+    _ok(lib.paged_kv_gather(_dptr(key_pool), _dptr(value_pool), key_pool.shape[0] // block_size, _dptr(block_table),
+                            B, W, int(first_block), int(n_blocks), _dptr(stage_k), _dptr(stage_v), stage_k.shape[1],
+                            hkv, d, dtype_code(key_pool), flags, _stream(stream)))
 
 
 def workspace_size(Tq: int, Hq: int, D: int, B: int, max_query_len: int, max_seq_len: int) -> int:

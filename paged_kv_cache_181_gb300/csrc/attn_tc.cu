@@ -49,6 +49,7 @@
 
 #include <cuda.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -87,6 +88,7 @@ struct alignas(1024) TcSmem {
 struct TcMaps {
   CUtensorMap q;       // (D, Hq, Tq), box = 64 columns x 128 tokens of one head
   CUtensorMap kb, vb;  // 5-D pool views, box = one whole 16-row pool block of one head
+  CUtensorMap kc, vc;  // the same views, box = 8 consecutive blocks = one whole key tile (contiguous K/V)
   CUtensorMap k1, v1;  // 3-D pool views (D, Hkv, slots), box = 64 columns of one row (partial blocks)
 };
 
@@ -110,16 +112,36 @@ PKV_DEVINLINE bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort
 }
 
 // Producer: gather key rows [kt*BN, kt*BN + rows) of one (row, kv head) into a slot.
+// Contiguous K/V (the row's table entries are consecutive): a whole tile is one box of
+// 8 blocks, which lands in the same [row group][column half][8 rows][128 B] layout.
 template <int D>
-PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensorMap* m1, uint64_t* full,
-                             const PkvAttnArgs& a, int b, int kvh, int kt, int rows, int lane) {
+PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensorMap* mc, const CUtensorMap* m1,
+                             uint64_t* full, const PkvAttnArgs& a, int b, int kvh, int kt, int rows, int lane) {
+  const int32_t* trow = a.block_table + (int64_t)b * a.W + kt * (BN / 16);
+  if (a.contiguous && rows == BN) {
+    int first = trow[0];
+    bool ok = true;
+    if (a.check) {
+      const int e = lane < BN / 16 ? trow[lane] : first + lane;
+      ok = __all_sync(0xffffffffu, e == first + lane) && first >= 0 && first <= a.num_blocks - BN / 16;
+      if (!ok && lane == 0) pkv_raise(a.err, PKV_DEVERR_BLOCK);  // not consecutive: fall through to blocks
+    }
+    if (ok) {
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(full, (uint32_t)(BN * D * 2));
+        ptx::tma_load_5d(dst, mc, 0, 0, 0, first * 2, kvh, full);
+      }
+      __syncwarp();
+      return;
+    }
+  }
   const int n_pages = (rows + 15) >> 4;
   const int rem = rows & 15;
   if (lane == 0) ptx::mbar_arrive_expect_tx(full, (uint32_t)(rows * D * 2));
   __syncwarp();
   if (lane < n_pages) {
     const int p = lane;
-    int blk = a.block_table[(int64_t)b * a.W + kt * (BN / 16) + p];
+    int blk = trow[p];
     if (a.check && (blk < 0 || blk >= a.num_blocks)) {
       pkv_raise(a.err, PKV_DEVERR_BLOCK);
       blk = 0;
@@ -196,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&maps.kb);
     ptx::prefetch_tmap(&maps.vb);
+    if (a.contiguous) {
+      ptx::prefetch_tmap(&maps.kc);
+      ptx::prefetch_tmap(&maps.vc);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -274,9 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (is_v)
-        load_tile<D>(sm.kv[pos], &maps.vb, &maps.v1, &sm.full[pos], a, b, kvh, kt, rows, lane);
+        load_tile<D>(sm.kv[pos], &maps.vb, &maps.vc, &maps.v1, &sm.full[pos], a, b, kvh, kt, rows, lane);
       else
-        load_tile<D>(sm.kv[pos], &maps.kb, &maps.k1, &sm.full[pos], a, b, kvh, kt, rows, lane);
+        load_tile<D>(sm.kv[pos], &maps.kb, &maps.kc, &maps.k1, &sm.full[pos], a, b, kvh, kt, rows, lane);
     }
     if (sm.abort && lane == 0) {
       // Let copies already issued land before the shared memory goes away.
@@ -538,6 +564,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, 
 template <int D, bool BF16>
 int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
   const int64_t num_slots = a.num_blocks * 16;
   const cuuint64_t slot = (cuuint64_t)a.Hkv * D * 2;
   // Pool as 5-D: (64 columns, 8 rows, D/64 column halves, slot groups of 8, heads),
@@ -545,6 +572,7 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   const cuuint64_t dims5[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(num_slots / 8), (cuuint64_t)a.Hkv};
   const cuuint64_t str5[4] = {slot, 128, 8 * slot, (cuuint64_t)D * 2};
   const cuuint32_t box5[5] = {64, 8, (cuuint32_t)(D / 64), 2, 1};
+  const cuuint32_t box5c[5] = {64, 8, (cuuint32_t)(D / 64), 2 * (BN / 16), 1};
   const cuuint64_t dims3[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)num_slots};
   const cuuint64_t str3[2] = {(cuuint64_t)D * 2, slot};
   const cuuint32_t box1[3] = {64, 1, 1};
@@ -552,6 +580,8 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   const cuuint64_t strq[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
   const cuuint32_t boxq[3] = {64, 1, BM};
   if (!encode(&maps.kb, a.k_pool, 5, dims5, str5, box5, BF16) || !encode(&maps.vb, a.v_pool, 5, dims5, str5, box5, BF16) ||
+      (a.contiguous && (!encode(&maps.kc, a.k_pool, 5, dims5, str5, box5c, BF16) ||
+                        !encode(&maps.vc, a.v_pool, 5, dims5, str5, box5c, BF16))) ||
       !encode(&maps.k1, a.k_pool, 3, dims3, str3, box1, BF16) || !encode(&maps.v1, a.v_pool, 3, dims3, str3, box1, BF16) ||
       !encode(&maps.q, a.q, 3, dimsq, strq, boxq, BF16))
     return (int)cudaErrorInvalidValue;

@@ -97,6 +97,40 @@ extern "C" pkv_status paged_kv_write(const void* k, const void* v, const int64_t
   return PKV_OK;
 }
 
+extern "C" pkv_status paged_kv_gather(const void* key_pool, const void* value_pool, int64_t num_blocks,
+                                      const int32_t* block_table, int B, int W, int first_block, int n_blocks,
+                                      void* stage_k, void* stage_v, int64_t stage_rows, int Hkv, int D, pkv_dtype dt,
+                                      uint32_t flags, void* stream) {
+  pkv_clear_error();
+  pkv_set_launches(0);
+  if (B < 0 || W < 0 || first_block < 0 || n_blocks < 0 || num_blocks < 0 || stage_rows < 0 || Hkv <= 0 || D <= 0)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: negative or zero size");
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_kv_gather: unknown dtype %d", (int)dt);
+  if ((int64_t)first_block + n_blocks > W)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: blocks [%d, %d) run past the table width %d", first_block,
+                    first_block + n_blocks, W);
+  if (((int64_t)first_block + n_blocks) * 16 > stage_rows)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: %d blocks do not fit %lld staging rows",
+                    first_block + n_blocks, (long long)stage_rows);
+  if ((int64_t)B * n_blocks * 32 >= ((int64_t)1 << 31))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: %d rows x %d blocks is too many for one call", B, n_blocks);
+  if (B == 0 || n_blocks == 0) return PKV_OK;
+  if (!key_pool || !value_pool || !block_table || !stage_k || !stage_v)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: NULL pointer");
+  const int64_t row_bytes = (int64_t)Hkv * D * pkv_dtype_size(dt);
+  if (row_bytes % 16 || !aligned16(key_pool) || !aligned16(value_pool) || !aligned16(stage_k) || !aligned16(stage_v))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_kv_gather: rows and base pointers must be 16-byte aligned");
+  const int check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
+  unsigned int* err = check ? pkv_device_error_word() : nullptr;
+  if (check && !err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_gather: device error word unavailable");
+  const int rc = pkv_launch_kv_gather(key_pool, value_pool, num_blocks, block_table, B, W, first_block, n_blocks,
+                                      stage_k, stage_v, stage_rows, (int)row_bytes, err, check, stream);
+  if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_kv_gather: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+  pkv_set_launches(1);
+  return PKV_OK;
+}
+
 namespace {
 
 // Split the key range only when the grid would otherwise leave SMs idle.
@@ -183,6 +217,7 @@ extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const
   a.max_seq_len = max_seq_len;
   a.scale = softmax_scale;
   a.check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
+  a.contiguous = (flags & PKV_CONTIGUOUS_KV) ? 1 : 0;
   // The error word is always passed: the tensor-core kernel reports pipeline timeouts through it.
   a.err = pkv_device_error_word();
   if (!a.err) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: device error word unavailable");

@@ -36,12 +36,16 @@ struct PkvAttnArgs {
   int max_query_len, max_seq_len;
   int num_splits;
   int check;
+  int contiguous;  // PKV_CONTIGUOUS_KV
   float scale;
 };
 
 // Launchers (each returns cudaGetLastError() as an int, 0 == success).
 int pkv_launch_kv_write(const void* k, const void* v, const int64_t* slots, int64_t T, void* kp, void* vp,
                         int64_t num_slots, int row_bytes, unsigned int* err, int check, void* stream);
+int pkv_launch_kv_gather(const void* kp, const void* vp, int64_t num_blocks, const int32_t* table, int B, int W,
+                          int first_block, int n_blocks, void* sk, void* sv, int64_t stage_rows, int row_bytes,
+                          unsigned int* err, int check, void* stream);
 int pkv_launch_attn_simt(const PkvAttnArgs& a, pkv_dtype dt, void* stream);
 int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream);
 // tcgen05 path; returns -1 when the shape is not handled by it.

@@ -65,3 +65,62 @@ int pkv_launch_kv_write(const void* k, const void* v, const int64_t* slots, int6
       (const uint4*)k, (const uint4*)v, slots, T, (uint4*)kp, (uint4*)vp, num_slots, vec_per_row, err, check);
   return (int)cudaGetLastError();
 }
+
+// ---------------------------------------------------------------- block gather into staging
+//
+// stage[b][first*16 + t] = pool[table[b][first + t/16]*16 + t%16] for K and V (paged_attention.py,
+// _stage_window).  Same shape as the write: one warp per (row b, token t, K|V) destination row.
+namespace {
+
+__global__ void __launch_bounds__(kThreads) kv_gather_kernel(const uint4* __restrict__ kp, const uint4* __restrict__ vp,
+                                                             int64_t num_blocks, const int32_t* __restrict__ table,
+                                                             int B, int W, int first_block, int n_blocks,
+                                                             uint4* __restrict__ sk, uint4* __restrict__ sv,
+                                                             int64_t stage_rows, int vec_per_row, unsigned int* err,
+                                                             int check) {
+  // The host keeps B * n_blocks * 32 below 2^31, so the row arithmetic stays in 32 bits.
+  const int lane = threadIdx.x & 31;
+  const int n_warps = gridDim.x * kWarps;
+  const int per_row = n_blocks * 16;
+  const int rows = B * per_row * 2;
+  for (int w = blockIdx.x * kWarps + (threadIdx.x >> 5); w < rows; w += n_warps) {
+    const bool is_v = w & 1;
+    const int bt = w >> 1;
+    const int b = bt / per_row;
+    const int t = bt - b * per_row;
+    int blk = __ldg(table + (int64_t)b * W + first_block + (int)(t >> 4));
+    if (check && (blk < 0 || blk >= num_blocks)) {
+      if (lane == 0) pkv_raise(err, PKV_DEVERR_BLOCK);
+      continue;
+    }
+    const uint4* src = (is_v ? vp : kp) + ((int64_t)blk * 16 + (t & 15)) * vec_per_row;
+    uint4* dst = (is_v ? sv : sk) + ((int64_t)b * stage_rows + (int64_t)first_block * 16 + t) * vec_per_row;
+    int c = lane;
+    for (; c + 32 * (kUnroll - 1) < vec_per_row; c += 32 * kUnroll) {
+      uint4 x[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) x[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) dst[c + 32 * u] = x[u];
+    }
+    for (; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+}  // namespace
+
+int pkv_launch_kv_gather(const void* kp, const void* vp, int64_t num_blocks, const int32_t* table, int B, int W,
+                         int first_block, int n_blocks, void* sk, void* sv, int64_t stage_rows, int row_bytes,
+                         unsigned int* err, int check, void* stream) {
+  const int vec_per_row = row_bytes / 16;
+  int sms = pkv_sm_count();
+  if (sms <= 0) sms = 152;
+  int64_t grid = ((int64_t)B * n_blocks * 32 + kWarps - 1) / kWarps;
+  const int64_t cap = (int64_t)sms * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  kv_gather_kernel<<<(unsigned)grid, kThreads, 0, (cudaStream_t)stream>>>(
+      (const uint4*)kp, (const uint4*)vp, num_blocks, table, B, W, first_block, n_blocks, (uint4*)sk, (uint4*)sv,
+      stage_rows, vec_per_row, err, check);
+  return (int)cudaGetLastError();
+}

@@ -70,6 +70,15 @@ def _pinned_to(a: np.ndarray, device) -> torch.Tensor:
 
 
 @dataclass
+class Staging:
+    k: torch.Tensor            # [B, W*16, Hkv, D]
+    v: torch.Tensor
+    table: torch.Tensor        # [B, W] int32, consecutive blocks of the staged rows
+    first_block: int           # first table entry a probe of the same chunk must re-gather
+    used_blocks: int           # table entries covering the longest row
+
+
+@dataclass
 class Case:
     w: Workload
     meta: Metadata
@@ -99,6 +108,41 @@ class Case:
             self.q[layer], self.k_pools[layer], self.v_pools[layer], self.block_table, self.query_start_loc,
             self.seq_lens, self.meta.max_query_len, self.meta.max_seq_len, self.scale, segs=self.segs,
             seg_start=self.seg_start, out=self.out[layer], workspace=self.workspace, flags=flags, stream=stream)
+
+    # ------------------------------------------------------------ contiguous K/V (staged window)
+
+    def make_staging(self) -> "Staging":
+        """Caller-owned contiguous buffers for one layer's visible window (``paged_attention.py``, the
+        history staging pairs): ``[B, W*16, Hkv, D]`` for K and V, and the table that reads them as
+        consecutive blocks (row ``b`` entry ``i`` = ``b*W + i``)."""
+        w, W = self.w, self.meta.width
+        dev = self.k_pools[0].device
+        shape = (w.batch, W * w.block_size, w.num_kv_heads, w.head_dim)
+        sk = torch.empty(shape, dtype=self.k_pools[0].dtype, device=dev)
+        sv = torch.empty_like(sk)
+        table = (torch.arange(w.batch, dtype=torch.int32, device=dev)[:, None] * W
+                 + torch.arange(W, dtype=torch.int32, device=dev)[None, :]).contiguous()
+        # Every block the current chunk's write can touch starts at the block of the first query
+        # token's kv position; the blocks before it hold history only.
+        first = int(min((int(L) - self.meta.max_query_len) // w.block_size for L in self.meta.seq_lens))
+        used = int(-(-int(self.meta.seq_lens.max()) // w.block_size))
+        return Staging(sk, sv, table, max(0, first), used)
+
+    def stage(self, layer: int, st: "Staging", reuse_history: bool = False, flags: int = 0, stream=None) -> None:
+        """Gather the layer's visible blocks into ``st``; with ``reuse_history`` only from the chunk's first block."""
+        first = st.first_block if reuse_history else 0
+        _lib.paged_kv_gather(self.k_pools[layer], self.v_pools[layer], self.block_table, st.k, st.v,
+                             first_block=first, n_blocks=st.used_blocks - first, flags=flags, stream=stream)
+
+    def attend_contiguous(self, layer: int, st: "Staging", flags: int = 0, stream=None) -> torch.Tensor:
+        """The same attention on the staged contiguous K/V (one TMA box per key tile)."""
+        w = self.w
+        kf = st.k.view(-1, w.num_kv_heads, w.head_dim)
+        vf = st.v.view(-1, w.num_kv_heads, w.head_dim)
+        return _lib.paged_attn_varlen(
+            self.q[layer], kf, vf, st.table, self.query_start_loc, self.seq_lens, self.meta.max_query_len,
+            self.meta.max_seq_len, self.scale, segs=self.segs, seg_start=self.seg_start, out=self.out[layer],
+            workspace=self.workspace, flags=flags | _lib.PKV_CONTIGUOUS_KV, stream=stream)
 
     def step(self, flags: int = 0, stream=None) -> None:
         """One forward: for every layer, write the chunk's K/V, then attend."""
