@@ -417,13 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = c < nvis ? s[c] : -INFINITY;
       }
+      // Row maximum: four chains of three-input maxima.
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 4; c < BN; c += 8) {
+        mx0 = ptx::max3(mx0, s[c], s[c + 1]);
+        mx1 = ptx::max3(mx1, s[c + 2], s[c + 3]);
+        mx2 = ptx::max3(mx2, s[c + 4], s[c + 5]);
+        mx3 = ptx::max3(mx3, s[c + 6], s[c + 7]);
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       // TMEM loads/stores are warp-collective: the warp rescales together when any
@@ -448,22 +449,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (need) m_ref = m_tile;
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      float l0 = 0.f, l1 = 0.f;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
       // P occupies columns [0, BN/2) of the score buffer: 32 scores -> 16 packed columns.
+      // Exponent arguments and partial sums run as packed fp32 pairs.
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ptx::ex2(fmaf(s[c * 32 + 2 * e], sl2, -mu));
-          const float p1 = ptx::ex2(fmaf(s[c * 32 + 2 * e + 1], sl2, -mu));
-          l0 += p0;
-          l1 += p1;
+          float x0, x1;
+          ptx::fma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, -mu, -mu);
+          const float p0 = ptx::ex2(x0);
+          const float p1 = ptx::ex2(x1);
+          if (e & 1)
+            ptx::add2(l2, l3, p0, p1);
+          else
+            ptx::add2(l0, l1, p0, p1);
           r[e] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
         }
         ptx::tmem_st16(tmem + lane_base + S_COL + c * 16, r);
       }
-      l += l0 + l1;
+      l += (l0 + l1) + (l2 + l3);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.p_full[grp]);

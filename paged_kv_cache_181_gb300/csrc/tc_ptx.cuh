@@ -337,6 +337,31 @@ PKV_DEVINLINE float ex2(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+PKV_DEVINLINE float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of fp32: (d0, d1) = (a0*b0 + c0, a1*b1 + c1), round-to-nearest, one instruction.
+PKV_DEVINLINE void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%6, %7};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Packed pairs of fp32: (d0, d1) += (a0, a1).
+PKV_DEVINLINE void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n.reg .b64 ra, rd;\n"
+      "mov.b64 ra, {%2, %3};\nmov.b64 rd, {%0, %1};\n"
+      "add.rn.f32x2 rd, rd, ra;\nmov.b64 {%0, %1}, rd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 PKV_DEVINLINE uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
