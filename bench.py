@@ -47,12 +47,18 @@ def load_peaks() -> dict:
 
 def visible_pairs(meta) -> int:
     """Visible (query, key) pairs summed over rows, from the library's host metadata."""
+    return pairs_from_segments(meta.query_start_loc, meta.seq_lens, meta.segments)
+
+
+def pairs_from_segments(query_start_loc, seq_lens, segments) -> int:
+    """Visible (query, key) pairs of rows given their (q_start, q_end, kv_end, mode) segments
+    (mode 1 = full); a row without segments sees all of its keys."""
     pairs = 0
-    for b in range(len(meta.seq_lens)):
-        sq = int(meta.query_start_loc[b + 1] - meta.query_start_loc[b])
-        L = int(meta.seq_lens[b])
+    for b in range(len(seq_lens)):
+        sq = int(query_start_loc[b + 1] - query_start_loc[b])
+        L = int(seq_lens[b])
         off = L - sq
-        segs = meta.segments[b] if meta.segments is not None and meta.segments[b] else [(off, L, L, 1)]
+        segs = segments[b] if segments is not None and segments[b] else [(off, L, L, 1)]
         for (s, e, kv_end, mode) in segs:
             n = e - s
             kv_end = min(kv_end, L)
@@ -329,6 +335,9 @@ def run_ours(args, world, rank, local):
     # Paged vs contiguous K/V on the same data (the pages' gather-then-attend path).
     kv_layout = measure_kv_layout(case, stream, attn_avg, row_bytes) if not args.no_kv_layout else None
 
+    # Packed heterogeneous rows: one call over rows of different shapes and query offsets.
+    packed_rows = measure_packed(stream, peaks) if not args.no_packed else None
+
     # e2e: inputs from pinned host memory every step, outputs back to the host.
     e2e = run_e2e(case, args, world, stream) if not args.no_e2e else None
 
@@ -353,6 +362,8 @@ def run_ours(args, world, rank, local):
         result["e2e"] = e2e
     if kv_layout is not None:
         result["kv_layout"] = kv_layout
+    if packed_rows is not None:
+        result["packed_rows"] = packed_rows
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = {k: v for k, v in cpu_oracle_sample(w).items() if k != "seconds"}
     if rank == 0:
@@ -360,6 +371,34 @@ def run_ours(args, world, rank, local):
 
 
 KERNEL_REV = "tc-v5-contig"
+
+
+def measure_packed(stream, peaks: dict, reps: int = 10) -> dict:
+    """TFLOP/s of one attention call over the packed heterogeneous rows (6 rows of the 832x480 model)."""
+    import torch
+
+    from paged_kv_cache_181_gb300 import configs, packed
+
+    pb = configs.PACKED_MIXED
+    pc = packed.build_packed(pb, poison=False)
+    flops = 4 * pb.head_dim * pb.num_heads * pairs_from_segments(pc.qsl_host, pc.seq_lens_host, pc.segments)
+    for _ in range(3):
+        pc.attend(stream=stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        pc.attend(stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    tflops = flops / (ms * 1e-3) / 1e12
+    res = {"workload": pb.name, "rows": len(pb.rows), "ms_per_launch": ms, "algorithmic_flops_per_launch": flops,
+           "achieved": tflops, "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+           "rows_desc": [[r.query_len, r.seq_len, r.kv_start_pos, len(r.spans)] for r in pb.rows]}
+    del pc
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
@@ -523,6 +562,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-layout", action="store_true", help="skip the paged vs contiguous K/V comparison")
+    ap.add_argument("--no-packed", action="store_true", help="skip the packed heterogeneous rows measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -13,7 +13,7 @@
  *   - piecewise_attn.py (vllm_omni/diffusion/attention/backends/utils):
  *       build_segments                -> build_segments
  *       piecewise_attn / module doc   -> the segment mask of paged_attn_varlen
- *       build_paged_piecewise_plan    -> span validation rules
+ *       build_paged_piecewise_plan    -> span validation rules; one query offset per packed row
  *   - paged_attention_adapter.py (vllm_omni/diffusion/diffusion_kv):
  *       head divisibility and query-is-a-suffix rules.
  *
@@ -230,8 +230,13 @@ PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int m
  *
  * Row b has Sq = query_start_loc[b+1] - query_start_loc[b] queries and
  * L = seq_lens[b] keys; key j of row b is pool row
- * block_table[b*W + j/16] * 16 + j % 16.  The query is the suffix of the key
- * sequence: local query i sits at global position L - Sq + i (Sq <= L).
+ * block_table[b*W + j/16] * 16 + j % 16.  Local query i sits at global position
+ * base_b + i: base_b is the q_start of the row's first segment when the row has
+ * segments (build_segments starts its cover at the query offset, so a packed row
+ * whose write span starts at kv_start_pos -- DiffusionPagedAttentionRow, with
+ * build_paged_piecewise_plan taking one query offset per row -- gets base_b =
+ * kv_start_pos), else the suffix convention base_b = L - Sq.  base_b + Sq <= L;
+ * check mode flags a row that breaks it (PKV_DEVERR_SEGMENT).
  * Query head h reads KV head h / (Hq / Hkv).
  *   segs, seg_start  device; segments of row b are segs[seg_start[b] .. seg_start[b+1]);
  *                    segs == NULL: every query sees all L keys (the pages' causal=False).

@@ -230,15 +230,20 @@ def paged_attention(
     *,
     dtype=np.float64,
     sample: dict | None = None,
+    query_offsets: Sequence[int] | None = None,
 ) -> np.ndarray:
     """Paged varlen attention with an optional piecewise causal/full mask per batch row.
 
     ``query`` is ``[Tq, Hq, D]`` packed by ``query_start_loc``; the pools are
     ``[num_blocks * bs, H_kv, D]``; ``block_table`` is ``[B, W]``.  For row ``b``
     with ``Sq`` queries and ``L = seq_lens[b]`` keys, the keys are gathered
-    through the block table and the query is the suffix of the key sequence, so
-    local query ``i`` sits at global position ``L - Sq + i`` (``piecewise_attn``
-    anchors the query at ``Skv - Sq``).
+    through the block table.  Local query ``i`` sits at global position
+    ``query_offsets[b] + i``; by default the query is the suffix of the key
+    sequence, ``query_offsets[b] = L - Sq`` (``piecewise_attn`` anchors the
+    query at ``Skv - Sq``).  Another offset is a packed row whose write span
+    starts at ``kv_start_pos`` (``DiffusionPagedAttentionRow``, with
+    ``build_paged_piecewise_plan`` taking one query offset per row); its
+    segments must come from ``build_segments`` with that offset.
 
     ``segments[b]`` (global coordinates, from ``build_segments``) splits row b's
     queries into causal and full pieces, each attended exactly as
@@ -262,7 +267,9 @@ def paged_attention(
             raise ValueError("the query must be a suffix of the key sequence (Sq <= seq_len)")
         k_all = gather_row_kv(key_pool, block_table[b], kv_len, block_size)
         v_all = gather_row_kv(value_pool, block_table[b], kv_len, block_size)
-        offset = kv_len - sq
+        offset = kv_len - sq if query_offsets is None else int(query_offsets[b])
+        if offset < 0 or offset + sq > kv_len:
+            raise ValueError("the row's query range must lie within its key sequence")
         row_segs = list(segments[b]) if segments is not None and segments[b] else [
             Segment(offset, kv_len, kv_len, FULL)
         ]
@@ -295,7 +302,8 @@ def paged_attention(
     return out
 
 
-def attention_flops(query_start_loc: Sequence[int], seq_lens: Sequence[int], segments, num_heads: int, head_dim: int) -> int:
+def attention_flops(query_start_loc: Sequence[int], seq_lens: Sequence[int], segments, num_heads: int, head_dim: int,
+                    query_offsets: Sequence[int] | None = None) -> int:
     """Algorithmic FLOPs: ``4 * D * Hq * (visible (query, key) pairs)``, summed over rows.
 
     Two multiply-adds per visible pair and head dimension: one for ``Q K^T``,
@@ -305,7 +313,7 @@ def attention_flops(query_start_loc: Sequence[int], seq_lens: Sequence[int], seg
     for b in range(len(seq_lens)):
         sq = int(query_start_loc[b + 1]) - int(query_start_loc[b])
         kv_len = int(seq_lens[b])
-        offset = kv_len - sq
+        offset = kv_len - sq if query_offsets is None else int(query_offsets[b])
         row_segs = list(segments[b]) if segments is not None and segments[b] else [
             Segment(offset, kv_len, kv_len, FULL)
         ]

@@ -95,3 +95,67 @@ LONG_WINDOW = Workload(
 )
 
 ALL = {w.name: w for w in (TINY, ONE_FRAME, ONE_FRAME_PARTIAL, GQA_ACTION, MIXED_MASK, LONG_WINDOW)}
+
+
+# ---------------------------------------------------------------- packed heterogeneous rows
+#
+# One attention call over rows that differ in query length, key length, spans and
+# query offset (paged_attention_adapter.py, DiffusionPagedAttentionRow: query_len,
+# seq_len, kv_start_pos; piecewise_attn.py, build_paged_piecewise_plan: one span list
+# and one query offset per packed row).  Every row's keys [0, seq_len) are written
+# into its own shuffled blocks of one shared pool.
+
+
+@dataclass(frozen=True)
+class PackedRow:
+    query_len: int
+    seq_len: int
+    kv_start_pos: int     # global key position of the row's first query token
+    spans: tuple = ()     # full-attention spans of this row (global key coordinates)
+
+
+@dataclass(frozen=True)
+class PackedBatch:
+    name: str
+    dtype: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    pool_blocks: int
+    sigma: float
+    seed: int
+    rows: tuple
+    notes: str = ""
+
+
+PACKED_SMALL = PackedBatch(
+    name="packed-small-bf16", dtype="bf16", num_heads=6, num_kv_heads=2, head_dim=128, block_size=16,
+    pool_blocks=256, sigma=1.0, seed=31,
+    rows=(
+        PackedRow(40, 40, 0, ((0, 40),)),                  # a first chunk, full inside itself
+        PackedRow(200, 900, 700, ((700, 900),)),           # a later chunk, suffix
+        PackedRow(130, 600, 200, ((200, 330),)),           # re-run mid-sequence: 270 keys after the query
+        PackedRow(1, 333, 332, ()),                        # one query token, causal
+        PackedRow(300, 300, 0, ()),                        # causal over everything
+        PackedRow(264, 777, 500, ((520, 600), (650, 700))),  # causal/full/causal/full/causal, not a suffix
+    ),
+    notes="6 rows: suffix and mid-sequence queries, 1..300 queries, 40..900 keys, GQA 3",
+)
+
+PACKED_MIXED = PackedBatch(
+    name="packed-mixed-bf16", dtype="bf16", num_heads=40, num_kv_heads=40, head_dim=128, block_size=16,
+    pool_blocks=4900, sigma=1.0, seed=32,
+    rows=(
+        PackedRow(1560, 1560, 0, ((0, 1560),)),                  # a new video's first frame
+        PackedRow(1560, 26520, 24960, ((24960, 26520),)),        # a long window (sink + 16 frames)
+        PackedRow(1568, 12488, 10920, ((10920, 12480),)),        # frame + 8 action tokens (causal tail)
+        PackedRow(1560, 14040, 6240, ((6240, 7800),)),           # a frame re-run mid-sequence
+        PackedRow(512, 4096, 3584, ()),                          # causal-only row
+        PackedRow(24, 18000, 17976, ()),                         # a short ragged tail
+    ),
+    notes="6 heterogeneous rows of the 832x480 model (40 heads, D=128): first frame, long window, "
+          "actions, mid-sequence re-run, causal, ragged tail",
+)
+
+PACKED = {p.name: p for p in (PACKED_SMALL, PACKED_MIXED)}

@@ -72,8 +72,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
         s_begin = a.seg_start[b];
         s_end = a.seg_start[b + 1];
       }
-      lim = pkv_row_limit(L - Sq + i, L, a.segs, s_begin, s_end, &uncovered);
-      if (a.check && uncovered) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
+      const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
+      lim = pkv_row_limit(base + i, L, a.segs, s_begin, s_end, &uncovered);
+      if (a.check && (uncovered || base < 0 || base + Sq > L)) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
     }
     lim_s[tid] = lim;
   }

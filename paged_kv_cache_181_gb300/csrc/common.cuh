@@ -36,6 +36,13 @@ PKV_DEVINLINE void pkv_raise(unsigned int* err, unsigned int bits) {
 // sees keys [0, limit).  Segments are the row's piecewise mask (global
 // coordinates): full -> kv_end; causal (bottom-right) -> kv_end - (q_end - p) + 1.
 // No segments -> L.  A row no segment covers sees nothing (and is flagged).
+// Global key position of a row's first query: the first segment's q_start when the row has
+// segments (build_segments starts its cover at the query offset, the row's kv_start_pos),
+// else the suffix convention L - Sq.
+PKV_DEVINLINE int pkv_query_base(int L, int Sq, const pkv_segment* segs, int s_begin, int s_end) {
+  return (segs != nullptr && s_begin < s_end) ? segs[s_begin].q_start : L - Sq;
+}
+
 PKV_DEVINLINE int pkv_row_limit(int p, int L, const pkv_segment* segs, int s_begin, int s_end, bool* uncovered) {
   if (segs == nullptr || s_begin >= s_end) return L;
   for (int s = s_begin; s < s_end; ++s) {

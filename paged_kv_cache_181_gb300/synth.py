@@ -91,3 +91,54 @@ def draw(w: Workload, layer: int = 0, device="cpu") -> Draw:
     k_cur = normal(tq, w.num_kv_heads, w.head_dim)
     v_cur = normal(tq, w.num_kv_heads, w.head_dim)
     return Draw(w, layer, row_blocks, action_blocks, q, k_hist, v_hist, k_cur, v_cur)
+
+
+# ---------------------------------------------------------------- packed heterogeneous rows
+
+
+@dataclass
+class PackedDraw:
+    batch: object            # configs.PackedBatch
+    row_blocks: list         # per row: int64 tensor, physical block of each logical block
+    q: torch.Tensor          # [sum query_len, Hq, D]
+    k_rows: list             # per row: [seq_len, Hkv, D]
+    v_rows: list
+
+
+def packed_allocation(pb):
+    """Per row, ``ceil(seq_len / bs)`` blocks from one permutation of blocks 1..pool_blocks-1
+    (CPU generator seeded ``seed * 1000 + 999``); block 0 stays the padding entry."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(pb.seed * 1000 + 999)
+    need = [_ceil_div(r.seq_len, pb.block_size) for r in pb.rows]
+    if sum(need) > pb.pool_blocks - 1:
+        raise ValueError(f"{pb.name}: pool of {pb.pool_blocks} blocks cannot hold {sum(need)} blocks")
+    perm = torch.randperm(pb.pool_blocks - 1, generator=g) + 1
+    out, used = [], 0
+    for n in need:
+        out.append(perm[used : used + n].clone())
+        used += n
+    return out
+
+
+def packed_draw(pb, device="cpu") -> PackedDraw:
+    """Q for every row's queries, then each row's K and V for all of its positions
+    (generator seeded ``seed * 1000``), ~ N(0, sigma), rounded to the batch dtype."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(pb.seed * 1000)
+    dt = TORCH_DTYPE[pb.dtype]
+
+    def normal(*shape):
+        x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+        if pb.sigma != 1.0:
+            x.mul_(pb.sigma)
+        return x.to(dt)
+
+    tq = sum(r.query_len for r in pb.rows)
+    q = normal(tq, pb.num_heads, pb.head_dim)
+    k_rows, v_rows = [], []
+    for r in pb.rows:
+        k_rows.append(normal(r.seq_len, pb.num_kv_heads, pb.head_dim))
+        v_rows.append(normal(r.seq_len, pb.num_kv_heads, pb.head_dim))
+    return PackedDraw(pb, packed_allocation(pb), q, k_rows, v_rows)

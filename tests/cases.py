@@ -126,3 +126,56 @@ EDGE = [
                         chunk_tokens=256, window_chunks=3, sink_chunks=0, history_tokens=512, query_tokens=256,
                         pool_blocks=128, seed=25),
 ]
+
+
+# ---------------------------------------------------------------- packed heterogeneous rows
+
+
+@dataclass
+class OraclePacked:
+    table: np.ndarray
+    seq_lens: np.ndarray
+    qsl: np.ndarray
+    offsets: np.ndarray
+    segments: list
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    q: np.ndarray
+
+
+def oracle_packed(pb, d: synth.PackedDraw) -> OraclePacked:
+    """Metadata and NaN-poisoned float32 pools of a packed batch, from oracle/ only."""
+    bs = pb.block_size
+    width = max(-(-r.seq_len // bs) for r in pb.rows)
+    table = np.zeros((len(pb.rows), width), dtype=np.int64)
+    kp = np.full((pb.pool_blocks * bs, pb.num_kv_heads, pb.head_dim), np.nan, dtype=np.float32)
+    vp = np.full_like(kp, np.nan)
+    segments = []
+    for b, r in enumerate(pb.rows):
+        blocks = [int(x) for x in d.row_blocks[b]]
+        table[b, : len(blocks)] = blocks
+        slots = pa.slot_mapping(blocks, range(r.seq_len), bs)
+        pa.kv_write(kp, slots, to_np(d.k_rows[b]))
+        pa.kv_write(vp, slots, to_np(d.v_rows[b]))
+        pa.validate_spans(list(r.spans), r.kv_start_pos, r.query_len, r.seq_len)
+        segments.append(pa.build_segments(list(r.spans), r.kv_start_pos, r.query_len))
+    seq_lens = np.array([r.seq_len for r in pb.rows], dtype=np.int64)
+    qsl = np.concatenate([[0], np.cumsum([r.query_len for r in pb.rows])]).astype(np.int64)
+    offsets = np.array([r.kv_start_pos for r in pb.rows], dtype=np.int64)
+    return OraclePacked(table, seq_lens, qsl, offsets, segments, kp, vp, to_np(d.q))
+
+
+def expected_packed(pb, op: OraclePacked, sample=None) -> np.ndarray:
+    return pa.paged_attention(op.q, op.k_pool, op.v_pool, op.table, op.qsl, op.seq_lens, pb.head_dim ** -0.5,
+                              pb.block_size, op.segments, sample=sample, query_offsets=op.offsets)
+
+
+def sample_packed_rows(pb, per_head: int, seed: int = 0) -> dict:
+    """Sampled local queries per (row, head): first, last, and random ones."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for b, r in enumerate(pb.rows):
+        for h in range(pb.num_heads):
+            extra = rng.choice(r.query_len, size=min(per_head, r.query_len), replace=False)
+            out[(b, h)] = np.array(sorted({0, r.query_len - 1} | set(int(x) for x in extra)), dtype=np.int64)
+    return out

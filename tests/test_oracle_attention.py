@@ -266,3 +266,33 @@ def test_attention_flops_count_visible_pairs():
         assert pa.attention_flops([0, sq], [L], [segs], 3, 8) == 4 * 8 * 3 * pairs
     # No segments: every key is visible.
     assert pa.attention_flops([0, 5], [9], None, 2, 4) == 4 * 4 * 2 * 45
+
+
+def test_rows_whose_query_is_not_a_suffix_match_sdpa():
+    # Packed rows carry their own query offset (kv_start_pos); keys after the query exist
+    # but only a full span reaching past the query makes them visible.
+    rng = np.random.default_rng(13)
+    cases = [
+        ([], 3, 5, 21),              # causal only: keys after the query stay hidden
+        ([(3, 8)], 3, 5, 21),        # full over exactly the query
+        ([(2, 19)], 3, 5, 21),       # a full span reaching past the query
+        ([(0, 4), (6, 12)], 2, 9, 30),
+        ([(10, 12)], 0, 16, 16),     # suffix case for comparison
+    ]
+    for spans, off, sq, L in cases:
+        kpool, vpool, table, k_rows, v_rows = make_paged(rng, [L], 2, 8, 8)
+        q = rng.standard_normal((sq, 4, 8))
+        segs = pa.build_segments(spans, off, sq)
+        out = pa.paged_attention(q, kpool, vpool, table, [0, sq], [L], 0.5, BS, [segs], query_offsets=[off])
+        want = sdpa(q, k_rows[0], v_rows[0], direct_mask(spans, off, sq, L), 0.5)
+        np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+        pairs = direct_mask(spans, off, sq, L).sum()
+        assert pa.attention_flops([0, sq], [L], [segs], 4, 8, query_offsets=[off]) == 4 * 8 * 4 * pairs
+
+
+def test_query_offset_outside_the_sequence_is_refused():
+    rng = np.random.default_rng(14)
+    kpool, vpool, table, _, _ = make_paged(rng, [10], 1, 4, 4)
+    q = rng.standard_normal((4, 1, 4))
+    with pytest.raises(ValueError):
+        pa.paged_attention(q, kpool, vpool, table, [0, 4], [10], 1.0, BS, None, query_offsets=[7])
