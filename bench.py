@@ -271,8 +271,10 @@ def run_ours(args, world, rank, local):
     write_bytes_per_layer = tq * 2 * (2 * row_bytes) + tq * 8  # read + write of K and V rows, plus the slot ids
     stream = torch.cuda.current_stream()
 
+    fused = not args.two_call
+
     def step():
-        case.step(stream=stream)
+        case.step(stream=stream, fused=fused)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -328,9 +330,13 @@ def run_ours(args, world, rank, local):
     write_avg = statistics.median(write_burst_ms)
     attn_tflops = flops_per_layer / (attn_avg * 1e-3) / 1e12
     write_gbs = write_bytes_per_layer / (write_avg * 1e-3) / 1e9
-    launches_per_step = sum(1 + attn_launches[l] for l in range(layers))
+    # Per layer: the attention launch (+ combine when split), plus the write launch in the two-call form.
+    launches_per_step = sum((0 if fused else 1) + attn_launches[l] for l in range(layers))
 
     traffic = read_traffic(w.name)
+
+    # The other way to run the same forward (two calls per layer, or the fused call).
+    alt = measure_alt_step(case, stream, args.steps, ms_step, not fused) if not args.no_alt else None
 
     # Paged vs contiguous K/V on the same data (the pages' gather-then-attend path).
     kv_layout = measure_kv_layout(case, stream, attn_avg, row_bytes) if not args.no_kv_layout else None
@@ -339,7 +345,7 @@ def run_ours(args, world, rank, local):
     packed_rows = measure_packed(stream, peaks) if not args.no_packed else None
 
     # e2e: inputs from pinned host memory every step, outputs back to the host.
-    e2e = run_e2e(case, args, world, stream) if not args.no_e2e else None
+    e2e = run_e2e(case, args, world, stream, fused) if not args.no_e2e else None
 
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -354,14 +360,19 @@ def run_ours(args, world, rank, local):
                      "algorithmic_flops_per_launch": flops_per_layer},
         "kv_write": {"bound": "hbm", "achieved": write_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": write_gbs / peaks["hbm_gbs"], "ms_per_launch": write_avg,
-                     "algorithmic_bytes_per_launch": write_bytes_per_layer},
+                     "algorithmic_bytes_per_launch": write_bytes_per_layer,
+                     "kernel": "paged_kv_write (standalone launch; inside the fused call it overlaps the attention)"},
         "gpu_launches": args.steps * launches_per_step,
+        "step_api": "paged_kv_write_attn per layer (write fused into the attention launch)" if fused
+                    else "paged_kv_write + paged_attn_varlen per layer",
         "clocks": clocks.summary(),
     }
     if e2e is not None:
         result["e2e"] = e2e
     if kv_layout is not None:
         result["kv_layout"] = kv_layout
+    if alt is not None:
+        result["fused" if not fused else "two_call"] = alt
     if packed_rows is not None:
         result["packed_rows"] = packed_rows
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -371,6 +382,26 @@ def run_ours(args, world, rank, local):
 
 
 KERNEL_REV = "tc-v5-contig"
+
+
+def measure_alt_step(case, stream, steps: int, main_ms_step: float, fused: bool) -> dict:
+    """Forward steps through the other API: paged_kv_write_attn (one launch per layer) or two calls."""
+    import torch
+
+    for _ in range(3):
+        case.step(stream=stream, fused=fused)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        case.step(stream=stream, fused=fused)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * case.layers
+    return {"api": "paged_kv_write_attn per layer" if fused else "paged_kv_write + paged_attn_varlen per layer",
+            "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "main_step_ms": main_ms_step, "main_over_this": main_ms_step / ms}
 
 
 def measure_packed(stream, peaks: dict, reps: int = 10) -> dict:
@@ -466,7 +497,7 @@ def read_traffic(workload_name: str):
     return int(m.group(3))
 
 
-def run_e2e(case, args, world, stream):
+def run_e2e(case, args, world, stream, fused: bool):
     """The same forward through the public API with every input coming from pinned host memory.
 
     Per step: the per-forward metadata and every layer's Q, new K and new V are copied host -> device on a
@@ -520,8 +551,11 @@ def run_e2e(case, args, world, stream):
         for l in range(layers):
             stream.wait_event(landed[l])
             stream.wait_event(fetched[l])  # the previous step's output of this layer has been read back
-            case.write(l, stream=stream)
-            case.attend(l, stream=stream)
+            if fused:
+                case.write_attend(l, stream=stream)
+            else:
+                case.write(l, stream=stream)
+                case.attend(l, stream=stream)
             computed[l].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(computed[l])
@@ -547,9 +581,9 @@ def run_e2e(case, args, world, stream):
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
     flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * layers * world
+    api = "paged_kv_write_attn" if fused else "paged_kv_write + paged_attn_varlen"
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps,
-            "api": "paged_kv_write + paged_attn_varlen per layer, inputs from pinned host memory"}
+            "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory"}
 
 
 def main():
@@ -563,6 +597,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kv-layout", action="store_true", help="skip the paged vs contiguous K/V comparison")
     ap.add_argument("--no-packed", action="store_true", help="skip the packed heterogeneous rows measurement")
+    ap.add_argument("--two-call", action="store_true",
+                    help="time the forward as paged_kv_write + paged_attn_varlen per layer (default: the fused call)")
+    ap.add_argument("--no-alt", action="store_true", help="skip timing the other API for comparison")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

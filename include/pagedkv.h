@@ -199,6 +199,31 @@ PKV_API pkv_status paged_kv_write(const void* k, const void* v, const int64_t* s
                           void* stream);
 
 /*
+ * paged_kv_write_attn -- paged_kv_write followed by paged_attn_varlen, in ONE launch
+ * (paged_attention.py, _paged_write_attn_impl: write the chunk's K/V into the pools, then
+ * attend through the block table).  The attention of the same launch reads the keys and
+ * values at the queries' own positions -- row b's keys [base_b, base_b + Sq), see
+ * paged_attn_varlen -- straight from k and v, while otherwise idle warps of the same CTAs
+ * scatter k and v into the pools; no CTA waits for the write.  The result equals the two
+ * calls in sequence when every token lands on the slot its key position implies:
+ *   slot_mapping[t] = block_table[b*W + key/16] * 16 + key % 16,  key = base_b + (t - query_start_loc[b])
+ * for the row b holding token t (what pkv_slot_mapping produces for the chunk).  Check mode
+ * verifies it and flags PKV_DEVERR_SLOT for a token that breaks it (that token is not written).
+ * A negative slot skips the token's write, as in paged_kv_write.
+ *   k, v          device [Tq, Hkv, D], dtype dt: the query tokens' keys and values
+ *   slot_mapping  device int64 [Tq]
+ *   everything else as paged_attn_varlen; key_pool/value_pool are written (num_blocks*16 slots).
+ * Tokens of different rows must not share pool blocks.  Splits add the combine launch.
+ */
+PKV_API pkv_status paged_kv_write_attn(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                                       int64_t Tq, int Hq, void* key_pool, void* value_pool, int64_t num_blocks,
+                                       int block_size, int Hkv, int D, pkv_dtype dt, const int32_t* block_table,
+                                       int B, int W, const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       int max_query_len, int max_seq_len, float softmax_scale,
+                                       const pkv_segment* segs, const int32_t* seg_start, void* out, void* workspace,
+                                       size_t ws_bytes, uint32_t flags, void* stream);
+
+/*
  * paged_kv_gather -- copy blocks [first_block, first_block + n_blocks) of every row's block table into
  * contiguous staging buffers: stage[b][first_block*16 + t] = pool[table[b*W + first_block + t/16]*16 + t%16]
  * for t < n_blocks*16, for K and V (paged_attention.py, _stage_window / the contiguous gather branch of

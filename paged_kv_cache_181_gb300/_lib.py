@@ -31,7 +31,7 @@ EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
     "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
     "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches", "paged_attn_varlen_noalloc",
-    "paged_kv_gather",
+    "paged_kv_gather", "paged_kv_write_attn",
 )
 
 
@@ -70,6 +70,9 @@ def _load() -> C.CDLL:
                                           i64p]),
         "paged_kv_write": (C.c_int, [vp, vp, vp, C.c_int64, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_uint32,
                                      vp]),
+        "paged_kv_write_attn": (C.c_int, [vp, vp, vp, vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int,
+                                          C.c_int, C.c_int, vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float,
+                                          vp, vp, vp, vp, C.c_size_t, C.c_uint32, vp]),
         "paged_kv_gather": (C.c_int, [vp, vp, C.c_int64, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, C.c_int64,
                                       C.c_int, C.c_int, C.c_int, C.c_uint32, vp]),
         "paged_attn_workspace_size": (C.c_size_t, [C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
@@ -252,6 +255,34 @@ def paged_attn_varlen(q, key_pool, value_pool, block_table, query_start_loc, seq
                               _dptr(seq_lens), int(max_query_len), int(max_seq_len), float(softmax_scale),
                               _dptr(segs), _dptr(seg_start), _dptr(out), _dptr(workspace), ws, flags,
                               _stream(stream)))
+    return out
+
+
+def paged_kv_write_attn(q, k, v, slot_mapping, key_pool, value_pool, block_table, query_start_loc, seq_lens,
+                        max_query_len: int, max_seq_len: int, softmax_scale: float, *, segs=None, seg_start=None,
+                        out=None, workspace=None, flags: int = 0, block_size: int = 16, stream=None):
+    """paged_kv_write + paged_attn_varlen in one launch (see include/pagedkv.h); returns ``out``."""
+    torch = _torch()
+    Tq, hq, d = q.shape
+    hkv = key_pool.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    for t in (q, k, v, slot_mapping, key_pool, value_pool, block_table, query_start_loc, seq_lens, out):
+        if not t.is_contiguous():
+            raise ValueError("paged_kv_write_attn: tensors must be contiguous")
+    if len({q.dtype, k.dtype, v.dtype, key_pool.dtype, value_pool.dtype, out.dtype}) != 1:
+        raise ValueError("paged_kv_write_attn: q, k, v, pools and out must share one dtype")
+    if k.shape != (Tq, hkv, d) or v.shape != k.shape:
+        raise ValueError("paged_kv_write_attn: k and v must be [Tq, Hkv, D]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != Tq:
+        raise ValueError("paged_kv_write_attn: slot_mapping must be int64 [Tq]")
+    B, W = block_table.shape
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok(lib.paged_kv_write_attn(_dptr(q), _dptr(k), _dptr(v), _dptr(slot_mapping), Tq, hq, _dptr(key_pool),
+                                _dptr(value_pool), key_pool.shape[0] // block_size, block_size, hkv, d, dtype_code(q),
+                                _dptr(block_table), B, W, _dptr(query_start_loc), _dptr(seq_lens),
+                                int(max_query_len), int(max_seq_len), float(softmax_scale), _dptr(segs),
+                                _dptr(seg_start), _dptr(out), _dptr(workspace), ws, flags, _stream(stream)))
     return out
 
 

@@ -13,7 +13,7 @@
 
 #include <math.h>
 
-#include "common.cuh"
+#include "kv_copy.cuh"
 
 namespace {
 
@@ -57,6 +57,15 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
       if (tid == 0 && tile == 0 && h == 0 && split == 0) pkv_raise(a.err, PKV_DEVERR_SEQLEN);
       L = L > lmax ? lmax : (L < 0 ? 0 : L);
     }
+  }
+  // Fused call: this CTA's share of the slot-mapping scatter, before its attention work.  The
+  // attention below reads the keys of the queries' own positions from the new tokens, so no CTA
+  // depends on the write.
+  if (a.k_new) {
+    const int64_t cta = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    pkv_scatter((const uint4*)a.k_new, (const uint4*)a.v_new, a.slots, a.Tq, (uint4*)a.k_pool, (uint4*)a.v_pool,
+                a.num_slots, a.Hkv * D * (int)sizeof(T) / 16, a.err, a.check, cta * kWarps + warp,
+                (int64_t)gridDim.x * gridDim.y * gridDim.z * kWarps, lane, &a);
   }
   const int i0 = tile * kQT;
   if (i0 >= Sq) return;
@@ -112,6 +121,17 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
 
   const T* kpool = (const T*)a.k_pool;
   const T* vpool = (const T*)a.v_pool;
+  // Keys at the queries' own positions [cb, ce): read from the new tokens in a fused call.
+  int cb = 0, ce = 0;
+  if (a.k_new) {
+    int s_begin = 0, s_end = 0;
+    if (a.segs) {
+      s_begin = a.seg_start[b];
+      s_end = a.seg_start[b + 1];
+    }
+    cb = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
+    ce = cb + Sq;
+  }
   for (int kt = t_begin; kt < t_end; ++kt) {
     const int j0 = kt * kKT;
     __syncthreads();
@@ -119,7 +139,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
     {
       const int jj = tid >> 2, part = tid & 3;
       const int j = j0 + jj;
-      if (j < kv_hi) {
+      if (j < kv_hi && j >= cb && j < ce) {
+        const int64_t tok = (int64_t)q0 + (j - cb);
+        load_row_f32<T>((const T*)a.k_new + (tok * a.Hkv + kvh) * D, k_s[jj], D, part, 4);
+        load_row_f32<T>((const T*)a.v_new + (tok * a.Hkv + kvh) * D, v_s[jj], D, part, 4);
+      } else if (j < kv_hi) {
         int blk = a.block_table[(int64_t)b * a.W + (j >> 4)];
         if (a.check && (blk < 0 || blk >= a.num_blocks)) {
           pkv_raise(a.err, PKV_DEVERR_BLOCK);

@@ -52,6 +52,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "kv_copy.cuh"
 #include "tc_ptx.cuh"
 
 namespace {
@@ -90,6 +91,14 @@ struct TcMaps {
   CUtensorMap kb, vb;  // 5-D pool views, box = one whole 16-row pool block of one head
   CUtensorMap kc, vc;  // the same views, box = 8 consecutive blocks = one whole key tile (contiguous K/V)
   CUtensorMap k1, v1;  // 3-D pool views (D, Hkv, slots), box = 64 columns of one row (partial blocks)
+  CUtensorMap kn5, vn5;  // fused call: new tokens in the pool's 5-D view, box = 16 tokens (8-aligned start)
+  CUtensorMap kn8, vn8;  //   (D, Hkv, Tq), box = 64 columns x 8 tokens (one atom)
+  CUtensorMap kn1, vn1;  //   the same, box = 64 columns of one token
+};
+
+// The maps one operand (K or V) is loaded through.
+struct OperandMaps {
+  const CUtensorMap *blk, *tile, *row, *new5, *new8, *new1;
 };
 
 // Byte offset of 128-byte row (tile row r, column half dh) in a key/value tile.
@@ -114,11 +123,15 @@ PKV_DEVINLINE bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort
 // Producer: gather key rows [kt*BN, kt*BN + rows) of one (row, kv head) into a slot.
 // Contiguous K/V (the row's table entries are consecutive): a whole tile is one box of
 // 8 blocks, which lands in the same [row group][column half][8 rows][128 B] layout.
+// Fused call: keys [cb, ce) -- the queries' own positions -- come from the new tokens
+// (token q0 + key - cb), whose write into the pool runs in the same launch.
 template <int D>
-PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensorMap* mc, const CUtensorMap* m1,
-                             uint64_t* full, const PkvAttnArgs& a, int b, int kvh, int kt, int rows, int lane) {
+PKV_DEVINLINE void load_tile(uint8_t* dst, const OperandMaps& m, uint64_t* full, const PkvAttnArgs& a, int b, int kvh,
+                             int kt, int rows, int cb, int ce, int q0, int lane) {
   const int32_t* trow = a.block_table + (int64_t)b * a.W + kt * (BN / 16);
-  if (a.contiguous && rows == BN) {
+  const int t0 = kt * BN;
+  const bool fused = a.k_new != nullptr;
+  if (a.contiguous && rows == BN && !(fused && t0 < ce && t0 + BN > cb)) {
     int first = trow[0];
     bool ok = true;
     if (a.check) {
@@ -129,32 +142,65 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const CUtensorMap* mb, const CUtensor
     if (ok) {
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(full, (uint32_t)(BN * D * 2));
-        ptx::tma_load_5d(dst, mc, 0, 0, 0, first * 2, kvh, full);
+        ptx::tma_load_5d(dst, m.tile, 0, 0, 0, first * 2, kvh, full);
       }
       __syncwarp();
       return;
     }
   }
   const int n_pages = (rows + 15) >> 4;
-  const int rem = rows & 15;
   if (lane == 0) ptx::mbar_arrive_expect_tx(full, (uint32_t)(rows * D * 2));
   __syncwarp();
   if (lane < n_pages) {
     const int p = lane;
-    int blk = trow[p];
-    if (a.check && (blk < 0 || blk >= a.num_blocks)) {
-      pkv_raise(a.err, PKV_DEVERR_BLOCK);
-      blk = 0;
+    const int k0 = t0 + 16 * p;                       // first key of this block
+    const int nr = rows - 16 * p < 16 ? rows - 16 * p : 16;  // its rows inside the tile
+    const bool all_new = fused && k0 >= cb && k0 + nr <= ce;
+    const bool no_new = !fused || k0 + nr <= cb || k0 >= ce;
+    int blk = 0;
+    if (!all_new) {
+      blk = trow[p];
+      if (a.check && (blk < 0 || blk >= a.num_blocks)) {
+        pkv_raise(a.err, PKV_DEVERR_BLOCK);
+        blk = 0;
+      }
     }
-    if (!(p == n_pages - 1 && rem != 0)) {
-      ptx::tma_load_5d(dst + tile_row_offset<D>(p * 16, 0), mb, 0, 0, 0, blk * 2, kvh, full);
-    } else {
-      for (int r = 0; r < rem; ++r)
+    if (nr == 16 && no_new) {
+      ptx::tma_load_5d(dst + tile_row_offset<D>(p * 16, 0), m.blk, 0, 0, 0, blk * 2, kvh, full);
+    } else if (nr == 16 && all_new && ((q0 + k0 - cb) & 7) == 0 && q0 + k0 - cb + 16 <= (int)(a.Tq & ~7ll)) {
+      // 16 new tokens starting on an 8-token boundary: one box, as for a pool block.
+      ptx::tma_load_5d(dst + tile_row_offset<D>(p * 16, 0), m.new5, 0, 0, 0, (q0 + k0 - cb) >> 3, kvh, full);
+    } else if (nr == 16 && all_new) {
+#pragma unroll
+      for (int at = 0; at < 2; ++at)
 #pragma unroll
         for (int dh = 0; dh < D / 64; ++dh)
-          ptx::tma_load_3d(dst + tile_row_offset<D>(p * 16 + r, dh), m1, dh * 64, kvh, blk * 16 + r, full);
+          ptx::tma_load_3d(dst + tile_row_offset<D>(p * 16 + 8 * at, dh), m.new8, dh * 64, kvh,
+                           q0 + (k0 + 8 * at - cb), full);
+    } else {
+      for (int r = 0; r < nr; ++r) {
+        const int key = k0 + r;
+        const bool from_new = fused && key >= cb && key < ce;
+#pragma unroll
+        for (int dh = 0; dh < D / 64; ++dh) {
+          if (from_new)
+            ptx::tma_load_3d(dst + tile_row_offset<D>(p * 16 + r, dh), m.new1, dh * 64, kvh, q0 + (key - cb), full);
+          else
+            ptx::tma_load_3d(dst + tile_row_offset<D>(p * 16 + r, dh), m.row, dh * 64, kvh, blk * 16 + r, full);
+        }
+      }
     }
   }
+}
+
+// Fused call: this CTA's share of the slot-mapping scatter, by warps 2 and 3 (idle otherwise).
+PKV_DEVINLINE void fused_write_share(const PkvAttnArgs& a, int warp, int lane) {
+  if (a.k_new == nullptr || (warp != 2 && warp != 3)) return;
+  const int64_t cta = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+  const int vec_per_row = a.Hkv * a.D * 2 / 16;
+  pkv_scatter((const uint4*)a.k_new, (const uint4*)a.v_new, a.slots, a.Tq, (uint4*)a.k_pool, (uint4*)a.v_pool,
+              a.num_slots, vec_per_row, a.err, a.check, cta * 2 + (warp - 2), (int64_t)gridDim.x * gridDim.y * 2, lane,
+              &a);
 }
 
 template <int D, bool BF16>
@@ -193,10 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   const int i0 = qp * 2 * BM;
-  if (i0 >= Sq) return;  // whole CTA: no query rows here
+  if (i0 >= Sq) {  // whole CTA: no query rows here
+    fused_write_share(a, warp, lane);
+    return;
+  }
   // A pipeline timeout earlier in this launch (or an unchecked earlier one) means
   // results are already invalid: fail fast instead of waiting again.
-  if (*(volatile unsigned int*)a.err & PKV_DEVERR_TIMEOUT) return;
+  if (*(volatile unsigned int*)a.err & PKV_DEVERR_TIMEOUT) {
+    fused_write_share(a, warp, lane);
+    return;
+  }
   const int n_q = i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
 
   // ---------------------------------------------------------------- set-up
@@ -221,6 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.contiguous) {
       ptx::prefetch_tmap(&maps.kc);
       ptx::prefetch_tmap(&maps.vc);
+    }
+    if (a.k_new) {
+      ptx::prefetch_tmap(&maps.kn8);
+      ptx::prefetch_tmap(&maps.vn8);
     }
   }
   if (warp == 1) {
@@ -268,6 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::regs_dec<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Keys at the queries' own positions [cb, ce) (fused call: read from the new tokens).
+    int cb = 0, ce = 0;
+    if (a.k_new) {
+      int s_begin = 0, s_end = 0;
+      if (a.segs) {
+        s_begin = a.seg_start[b];
+        s_end = a.seg_start[b + 1];
+      }
+      cb = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
+      ce = cb + Sq;
+      cb = cb < 0 ? 0 : cb;
+      ce = ce > L ? L : ce;
+    }
+    const OperandMaps km{&maps.kb, &maps.kc, &maps.k1, &maps.kn5, &maps.kn8, &maps.kn1};
+    const OperandMaps vm{&maps.vb, &maps.vc, &maps.v1, &maps.vn5, &maps.vn8, &maps.vn1};
     if (n > 0) {
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(n_q * BM * D * 2));
@@ -300,10 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
       }
-      if (is_v)
-        load_tile<D>(sm.kv[pos], &maps.vb, &maps.vc, &maps.v1, &sm.full[pos], a, b, kvh, kt, rows, lane);
-      else
-        load_tile<D>(sm.kv[pos], &maps.kb, &maps.kc, &maps.k1, &sm.full[pos], a, b, kvh, kt, rows, lane);
+      load_tile<D>(sm.kv[pos], is_v ? vm : km, &sm.full[pos], a, b, kvh, kt, rows, cb, ce, q0, lane);
     }
     if (sm.abort && lane == 0) {
       // Let copies already issued land before the shared memory goes away.
@@ -380,6 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dummy = 0;
       ptx::mbar_wait(&sm.mma_done, 0, &dummy, kWaitLimitNs);
     }
+  } else {
+    // ------------------------------------------------------------ warps 2-3: fused write
+    fused_write_share(a, warp, lane);
   }
   } else {
   ptx::regs_inc<kRegsHigh>();
@@ -592,6 +663,19 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
       !encode(&maps.k1, a.k_pool, 3, dims3, str3, box1, BF16) || !encode(&maps.v1, a.v_pool, 3, dims3, str3, box1, BF16) ||
       !encode(&maps.q, a.q, 3, dimsq, strq, boxq, BF16))
     return (int)cudaErrorInvalidValue;
+  if (a.k_new) {
+    // New tokens [Tq, Hkv, D]: (D, Hkv, Tq) with the pool's row stride.
+    const cuuint64_t dimsn[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)a.Tq};
+    const cuuint32_t boxn8[3] = {64, 1, 8};
+    if (!encode(&maps.kn8, a.k_new, 3, dimsn, str3, boxn8, BF16) || !encode(&maps.vn8, a.v_new, 3, dimsn, str3, boxn8, BF16) ||
+        !encode(&maps.kn1, a.k_new, 3, dimsn, str3, box1, BF16) || !encode(&maps.vn1, a.v_new, 3, dimsn, str3, box1, BF16))
+      return (int)cudaErrorInvalidValue;
+    if (a.Tq >= 16) {  // the kernel uses this view only for 16 tokens inside the first Tq & ~7
+      const cuuint64_t dimsn5[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(a.Tq / 8), (cuuint64_t)a.Hkv};
+      if (!encode(&maps.kn5, a.k_new, 5, dimsn5, str5, box5, BF16) || !encode(&maps.vn5, a.v_new, 5, dimsn5, str5, box5, BF16))
+        return (int)cudaErrorInvalidValue;
+    }
+  }
   const size_t smem = sizeof(TcSmem<D>) + 1024;
   static bool attr_set[64] = {};
   int dev = 0;

@@ -164,37 +164,43 @@ extern "C" size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, in
   return (size_t)kMaxSplits * (size_t)Tq * (size_t)Hq * ((size_t)D + 1) * sizeof(float);
 }
 
-extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const void* key_pool,
-                                        const void* value_pool, int64_t num_blocks, int block_size, int Hkv, int D,
-                                        pkv_dtype dt, const int32_t* block_table, int B, int W,
-                                        const int32_t* query_start_loc, const int32_t* seq_lens, int max_query_len,
-                                        int max_seq_len, float softmax_scale, const pkv_segment* segs,
-                                        const int32_t* seg_start, void* out, void* workspace, size_t ws_bytes,
-                                        uint32_t flags, void* stream) {
+namespace {
+
+struct FusedWrite {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+};
+
+pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const void* key_pool, const void* value_pool,
+                     int64_t num_blocks, int block_size, int Hkv, int D, pkv_dtype dt, const int32_t* block_table,
+                     int B, int W, const int32_t* query_start_loc, const int32_t* seq_lens, int max_query_len,
+                     int max_seq_len, float softmax_scale, const pkv_segment* segs, const int32_t* seg_start,
+                     void* out, void* workspace, size_t ws_bytes, uint32_t flags, void* stream, const FusedWrite* fw) {
   pkv_clear_error();
   pkv_set_launches(0);
   if (Tq < 0 || B < 0 || W < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0)
-    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: negative size");
+    return pkv_fail(PKV_ERR_INVALID_ARG, "%s: negative size", fn);
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv)
     return pkv_fail(PKV_ERR_INVALID_ARG,
-                    "paged_attn_varlen: num_heads must be a positive multiple of num_kv_heads (Hq=%d, Hkv=%d)", Hq, Hkv);
-  if (block_size != 16) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: block_size must be 16 (got %d)", block_size);
-  if (D != 64 && D != 128) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: head dim must be 64 or 128 (got %d)", D);
+                    "%s: num_heads must be a positive multiple of num_kv_heads (Hq=%d, Hkv=%d)", fn, Hq, Hkv);
+  if (block_size != 16) return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: block_size must be 16 (got %d)", fn, block_size);
+  if (D != 64 && D != 128) return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: head dim must be 64 or 128 (got %d)", fn, D);
   if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16)
-    return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen: unknown dtype %d", (int)dt);
-  if (!isfinite(softmax_scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: softmax_scale is not finite");
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dt);
+  if (!isfinite(softmax_scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: softmax_scale is not finite", fn);
   if ((int64_t)max_seq_len > (int64_t)W * block_size)
-    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: max_seq_len %d exceeds the table's %d x %d slots",
+    return pkv_fail(PKV_ERR_INVALID_ARG, "%s: max_seq_len %d exceeds the table's %d x %d slots", fn,
                     max_seq_len, W, block_size);
   if (Tq == 0 || B == 0 || max_query_len == 0) return PKV_OK;
   if (!q || !key_pool || !value_pool || !block_table || !query_start_loc || !seq_lens || !out)
-    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: NULL pointer");
-  if (segs && !seg_start) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: segs given without seg_start");
+    return pkv_fail(PKV_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (segs && !seg_start) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: segs given without seg_start", fn);
   if (!aligned16(q) || !aligned16(key_pool) || !aligned16(value_pool) || !aligned16(out))
-    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: q, pools and out must be 16-byte aligned");
+    return pkv_fail(PKV_ERR_INVALID_ARG, "%s: q, pools and out must be 16-byte aligned", fn);
   if (max_query_len > max_seq_len)
-    return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: max_query_len %d > max_seq_len %d (the query is a "
-                    "suffix of the key sequence)", max_query_len, max_seq_len);
+    return pkv_fail(PKV_ERR_INVALID_ARG, "%s: max_query_len %d > max_seq_len %d (the query is a "
+                    "suffix of the key sequence)", fn, max_query_len, max_seq_len);
 
   PkvAttnArgs a{};
   a.q = q;
@@ -220,7 +226,7 @@ extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const
   a.contiguous = (flags & PKV_CONTIGUOUS_KV) ? 1 : 0;
   // The error word is always passed: the tensor-core kernel reports pipeline timeouts through it.
   a.err = pkv_device_error_word();
-  if (!a.err) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: device error word unavailable");
+  if (!a.err) return pkv_fail(PKV_ERR_CUDA, "%s: device error word unavailable", fn);
 
   const bool use_tc = !(flags & PKV_FORCE_SIMT) && pkv_attn_tc_supports(dt, D);
   int sms = pkv_sm_count();
@@ -242,26 +248,62 @@ extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const
     const size_t need = (size_t)splits * (size_t)Tq * Hq * ((size_t)D + 1) * sizeof(float);
     if (!workspace || ws_bytes < need) {
       if (forced > 0)
-        return pkv_fail(PKV_ERR_CAPACITY, "paged_attn_varlen: %d splits need %zu workspace bytes, got %zu", splits,
+        return pkv_fail(PKV_ERR_CAPACITY, "%s: %d splits need %zu workspace bytes, got %zu", fn, splits,
                         need, ws_bytes);
       splits = 1;
     } else {
-      if (!aligned16(workspace)) return pkv_fail(PKV_ERR_INVALID_ARG, "paged_attn_varlen: workspace must be 16-byte aligned");
+      if (!aligned16(workspace)) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
       a.part_o = (float*)workspace;
       a.part_lse = a.part_o + (size_t)splits * Tq * Hq * D;
     }
   }
   a.num_splits = splits;
+  if (fw) {
+    if (!fw->k || !fw->v || !fw->slots) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: NULL k, v or slot_mapping", fn);
+    if (!aligned16(fw->k) || !aligned16(fw->v))
+      return pkv_fail(PKV_ERR_INVALID_ARG, "%s: k and v must be 16-byte aligned", fn);
+    a.k_new = fw->k;
+    a.v_new = fw->v;
+    a.slots = fw->slots;
+    a.num_slots = num_blocks * block_size;
+  }
 
   int rc = -1;
   if (use_tc) rc = pkv_launch_attn_tc(a, dt, stream);
   if (rc == -1) rc = pkv_launch_attn_simt(a, dt, stream);
-  if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+  if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString((cudaError_t)rc));
   if (splits > 1) {
     rc = pkv_launch_attn_combine(a, dt, stream);
     if (rc != 0)
-      return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen: combine launch failed: %s", cudaGetErrorString((cudaError_t)rc));
+      return pkv_fail(PKV_ERR_CUDA, "%s: combine launch failed: %s", fn, cudaGetErrorString((cudaError_t)rc));
   }
   pkv_set_launches(splits > 1 ? 2 : 1);
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const void* key_pool,
+                                        const void* value_pool, int64_t num_blocks, int block_size, int Hkv, int D,
+                                        pkv_dtype dt, const int32_t* block_table, int B, int W,
+                                        const int32_t* query_start_loc, const int32_t* seq_lens, int max_query_len,
+                                        int max_seq_len, float softmax_scale, const pkv_segment* segs,
+                                        const int32_t* seg_start, void* out, void* workspace, size_t ws_bytes,
+                                        uint32_t flags, void* stream) {
+  return attn_impl("paged_attn_varlen", q, Tq, Hq, key_pool, value_pool, num_blocks, block_size, Hkv, D, dt,
+                   block_table, B, W, query_start_loc, seq_lens, max_query_len, max_seq_len, softmax_scale, segs,
+                   seg_start, out, workspace, ws_bytes, flags, stream, nullptr);
+}
+
+extern "C" pkv_status paged_kv_write_attn(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                                          int64_t Tq, int Hq, void* key_pool, void* value_pool, int64_t num_blocks,
+                                          int block_size, int Hkv, int D, pkv_dtype dt, const int32_t* block_table,
+                                          int B, int W, const int32_t* query_start_loc, const int32_t* seq_lens,
+                                          int max_query_len, int max_seq_len, float softmax_scale,
+                                          const pkv_segment* segs, const int32_t* seg_start, void* out,
+                                          void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
+  const FusedWrite fw{k, v, slot_mapping};
+  return attn_impl("paged_kv_write_attn", q, Tq, Hq, key_pool, value_pool, num_blocks, block_size, Hkv, D, dt,
+                   block_table, B, W, query_start_loc, seq_lens, max_query_len, max_seq_len, softmax_scale, segs,
+                   seg_start, out, workspace, ws_bytes, flags, stream, &fw);
 }

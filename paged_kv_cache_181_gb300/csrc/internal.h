@@ -38,6 +38,13 @@ struct PkvAttnArgs {
   int check;
   int contiguous;  // PKV_CONTIGUOUS_KV
   float scale;
+  // Fused write (paged_kv_write_attn): the current tokens' K/V [Tq, Hkv, D] and their slots.
+  // The same launch scatters them into the pools and its attention reads the keys of the
+  // queries' own positions from here instead of the pools.  k_new == nullptr: no write.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+  int64_t num_slots;
 };
 
 // Launchers (each returns cudaGetLastError() as an int, 0 == success).

@@ -11,43 +11,21 @@
 // 64-bit division per vector measured 27.1 us per launch on the long-window
 // workload; this one 24.8 us, 76 % of the measured copy bandwidth.)
 
-#include "common.cuh"
+#include "kv_copy.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                             const int64_t* __restrict__ slots, int64_t T,
                                                             uint4* __restrict__ kp, uint4* __restrict__ vp,
                                                             int64_t num_slots, int vec_per_row, unsigned int* err,
                                                             int check) {
-  const int lane = threadIdx.x & 31;
-  const int64_t n_warps = (int64_t)gridDim.x * kWarps;
-  const int64_t rows = T * 2;
-  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += n_warps) {
-    const int64_t t = row >> 1;
-    const bool is_v = row & 1;
-    const int64_t s = __ldg(slots + t);
-    if (s < 0) continue;  // negative slot: skip the token
-    if (check && s >= num_slots) {
-      if (lane == 0) pkv_raise(err, PKV_DEVERR_SLOT);
-      continue;
-    }
-    const uint4* src = (is_v ? v : k) + t * vec_per_row;
-    uint4* dst = (is_v ? vp : kp) + s * vec_per_row;
-    int c = lane;
-    for (; c + 32 * (kUnroll - 1) < vec_per_row; c += 32 * kUnroll) {
-      uint4 x[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) x[u] = __ldg(src + c + 32 * u);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) dst[c + 32 * u] = x[u];
-    }
-    for (; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
-  }
+  pkv_scatter(k, v, slots, T, kp, vp, num_slots, vec_per_row, err, check,
+              (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5), (int64_t)gridDim.x * kWarps, threadIdx.x & 31,
+              nullptr);
 }
 
 }  // namespace
@@ -95,15 +73,7 @@ __global__ void __launch_bounds__(kThreads) kv_gather_kernel(const uint4* __rest
     }
     const uint4* src = (is_v ? vp : kp) + ((int64_t)blk * 16 + (t & 15)) * vec_per_row;
     uint4* dst = (is_v ? sv : sk) + ((int64_t)b * stage_rows + (int64_t)first_block * 16 + t) * vec_per_row;
-    int c = lane;
-    for (; c + 32 * (kUnroll - 1) < vec_per_row; c += 32 * kUnroll) {
-      uint4 x[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) x[u] = __ldg(src + c + 32 * u);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) dst[c + 32 * u] = x[u];
-    }
-    for (; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
+    pkv_copy_row(src, dst, vec_per_row, lane);
   }
 }
 

@@ -144,11 +144,22 @@ class Case:
             self.meta.max_seq_len, self.scale, segs=self.segs, seg_start=self.seg_start, out=self.out[layer],
             workspace=self.workspace, flags=flags | _lib.PKV_CONTIGUOUS_KV, stream=stream)
 
-    def step(self, flags: int = 0, stream=None) -> None:
-        """One forward: for every layer, write the chunk's K/V, then attend."""
+    def write_attend(self, layer: int, flags: int = 0, stream=None) -> torch.Tensor:
+        """The layer's write and attention in one launch (attention reads the chunk from k/v)."""
+        return _lib.paged_kv_write_attn(
+            self.q[layer], self.k_new[layer], self.v_new[layer], self.slots, self.k_pools[layer], self.v_pools[layer],
+            self.block_table, self.query_start_loc, self.seq_lens, self.meta.max_query_len, self.meta.max_seq_len,
+            self.scale, segs=self.segs, seg_start=self.seg_start, out=self.out[layer], workspace=self.workspace,
+            flags=flags, stream=stream)
+
+    def step(self, flags: int = 0, stream=None, fused: bool = False) -> None:
+        """One forward: for every layer, write the chunk's K/V, then attend (``fused``: one launch)."""
         for layer in range(self.layers):
-            self.write(layer, flags, stream)
-            self.attend(layer, flags, stream)
+            if fused:
+                self.write_attend(layer, flags, stream)
+            else:
+                self.write(layer, flags, stream)
+                self.attend(layer, flags, stream)
 
 
 def build_case(w: Workload, device="cuda", layers: int | None = None, poison: bool = False,
