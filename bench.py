@@ -381,7 +381,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v5-contig"
+KERNEL_REV = "tc-v6-fused"
 
 
 def measure_alt_step(case, stream, steps: int, main_ms_step: float, fused: bool) -> dict:

@@ -96,6 +96,16 @@ struct TcMaps {
   CUtensorMap kn1, vn1;  //   the same, box = 64 columns of one token
 };
 
+// Work items (one CTA each, in launch order): pairs of 128-query tiles of one (row, query head),
+// then single tiles -- the last `split` pairs broken in two, and each (row, head)'s odd last tile.
+// Blocks start in index order as SMs free up, so the cheaper single-tile CTAs fill the last wave.
+struct TcSched {
+  int n_t;     // query tiles per (row, head): ceil(max_query_len / 128)
+  int np;      // tile pairs per (row, head): n_t / 2
+  int pairs;   // B * Hq * np
+  int split;   // trailing pairs issued as two single-tile items
+};
+
 // The maps one operand (K or V) is loaded through.
 struct OperandMaps {
   const CUtensorMap *blk, *tile, *row, *new5, *new8, *new1;
@@ -205,21 +215,37 @@ PKV_DEVINLINE void fused_write_share(const PkvAttnArgs& a, int warp, int lane) {
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ TcMaps maps, const PkvAttnArgs a) {
+    attn_tc_kernel(const __grid_constant__ TcMaps maps, const PkvAttnArgs a, const TcSched sc) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = a.Hq / a.Hkv;
-  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
-  int u = blockIdx.x;
-  const int gi = u % g;
-  u /= g;
-  const int qp = u % n_qp;
-  u /= n_qp;
-  const int kvh = u % a.Hkv;
-  const int b = u / a.Hkv;
+  // Decode the work item: (row b, kv head, group member gi, first tile t0, tiles nt).
+  int gi, kvh, b, t0, nt;
+  {
+    const int item = blockIdx.x;
+    const int direct = sc.pairs - sc.split;
+    int u, p = 0;
+    if (item < direct + 2 * sc.split) {  // a pair, or half of a split pair
+      u = item < direct ? item : direct + ((item - direct) >> 1);
+      gi = u % g;
+      u /= g;
+      p = u % sc.np;
+      u /= sc.np;
+      t0 = 2 * p + (item < direct ? 0 : ((item - direct) & 1));
+      nt = item < direct ? 2 : 1;
+    } else {  // the odd last tile of a (row, head)
+      u = item - direct - 2 * sc.split;
+      gi = u % g;
+      u /= g;
+      t0 = sc.n_t - 1;
+      nt = 1;
+    }
+    kvh = u % a.Hkv;
+    b = u / a.Hkv;
+  }
   const int h = kvh * g + gi;
   const int split = blockIdx.y;
 
@@ -228,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int L = a.seq_lens[b];
   if (a.check) {
     const int lmax = a.W * 16 < a.max_seq_len ? a.W * 16 : a.max_seq_len;
-    const bool first = tid == 0 && qp == 0 && gi == 0 && split == 0;
+    const bool first = tid == 0 && t0 == 0 && gi == 0 && split == 0;
     if (Sq < 0 || Sq > a.max_query_len) {
       if (first) pkv_raise(a.err, PKV_DEVERR_QUERY);
       Sq = Sq < 0 ? 0 : a.max_query_len;
@@ -238,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       L = L > lmax ? lmax : (L < 0 ? 0 : L);
     }
   }
-  const int i0 = qp * 2 * BM;
+  const int i0 = t0 * BM;
   if (i0 >= Sq) {  // whole CTA: no query rows here
     fused_write_share(a, warp, lane);
     return;
@@ -249,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fused_write_share(a, warp, lane);
     return;
   }
-  const int n_q = i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
+  const int n_q = nt == 2 && i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -391,27 +417,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         return true;
       };
+      // One issuing thread feeds the tensor core: an MMA (128x128x16) takes 64 cycles, so the
+      // descriptors are built once and each MMA only offsets one (ptx::desc_add).  Rebuilding
+      // them per MMA measured a third slower when Q.K^T and P.V alternate.
+      // Q: [half][128 rows][128 B] -> 8-row atoms at 1024 B, column half at BM*128 B.
+      const uint64_t q_desc[2] = {ptx::smem_desc(q_base[0], 16, 1024, 2), ptx::smem_desc(q_base[1], 16, 1024, 2)};
+      // K: block-interleaved -> 8-row atoms at GS, column half at +1024 B.  V: MN-major.
+      const uint64_t k_desc = ptx::smem_desc(kv_base, 16, C::GS, 2);
+      const uint64_t v_desc = ptx::smem_desc(kv_base, 1024, C::GS, 2);
       // S_w = Q_w K_j^T (key tile j sits in slot (2j) % NSLOT)
       auto qk = [&](int w, int j) {
-        const uint32_t kst = kv_base + ((2 * j) % C::NSLOT) * C::TILE;
+        const uint64_t kd = ptx::desc_add(k_desc, (uint32_t)(((2 * j) % C::NSLOT) * C::TILE) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // Q: [half][128 rows][128 B] -> 8-row atoms at 1024 B, column half at BM*128 B
-          const uint64_t adesc = ptx::smem_desc(q_base[w] + (ks >> 2) * (BM * 128) + (ks & 3) * 32, 16, 1024, 2);
-          // K: block-interleaved -> 8-row atoms at GS, column half at +1024 B
-          const uint64_t bdesc = ptx::smem_desc(kst + (ks >> 2) * 1024 + (ks & 3) * 32, 16, C::GS, 2);
-          ptx::mma_ss(tmem + 128 * w, adesc, bdesc, IDESC_QK, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_ss(tmem + 128 * w, ptx::desc_add(q_desc[w], ((ks >> 2) * (BM * 128) + (ks & 3) * 32) >> 4),
+                      ptx::desc_add(kd, ((ks >> 2) * 1024 + (ks & 3) * 32) >> 4), IDESC_QK, ks > 0);
         ptx::mma_commit(&sm.s_full[w]);
       };
       // O_w (+)= P_w V_j (value tile j sits in slot (2j+1) % NSLOT; P_w over the first columns of S_w)
       auto pv = [&](int w, int j) {
-        const uint32_t vst = kv_base + ((2 * j + 1) % C::NSLOT) * C::TILE;
+        const uint64_t vd = ptx::desc_add(v_desc, (uint32_t)(((2 * j + 1) % C::NSLOT) * C::TILE) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = ptx::smem_desc(vst + ks * (2 * C::GS), 1024, C::GS, 2);
-          ptx::mma_ts(tmem + O_COL[w], tmem + 128 * w + ks * 8, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          ptx::mma_ts(tmem + O_COL[w], tmem + 128 * w + ks * 8, ptx::desc_add(vd, (ks * 2 * C::GS) >> 4), IDESC_PV,
+                      (j > 0 || ks > 0) ? 1u : 0u);
       };
       if (ok) ok = slot_ready(0);
       if (ok) {
@@ -691,11 +720,23 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
     attr_set[dev] = true;
   }
   const int g = a.Hq / a.Hkv;
-  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
-  const int64_t ctas = (int64_t)a.B * a.Hkv * n_qp * g;
-  if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
+  const int64_t heads = (int64_t)a.B * a.Hq;
+  TcSched sc{};
+  sc.n_t = (a.max_query_len + BM - 1) / BM;
+  sc.np = sc.n_t / 2;
+  const int64_t pairs = heads * sc.np, odd = heads * (sc.n_t & 1);
+  if (pairs + odd > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
+  sc.pairs = (int)pairs;
+  // Break the pairs left over after the last full wave into single tiles when those and the odd
+  // tiles fit in one wave: a single-tile CTA takes about 0.6 of a pair's time (it still streams
+  // every key), so the last wave ends sooner.
+  int sms = pkv_sm_count();
+  if (sms <= 0) sms = 152;
+  const int64_t rem = pairs % sms;
+  sc.split = (a.num_splits == 1 && rem > 0 && 2 * rem + odd <= sms) ? (int)rem : 0;
+  const int64_t ctas = pairs + sc.split + odd;
   dim3 grid((unsigned)ctas, (unsigned)a.num_splits);
-  attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a);
+  attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a, sc);
   return (int)cudaGetLastError();
 }
 

@@ -321,6 +321,14 @@ PKV_DEVINLINE uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sb
 
 // Instruction descriptor, kind::f16 with fp32 accumulation.
 //   ab_bf16: 1 = bf16 operands, 0 = f16;  b_mn_major: 1 = B is MN-major.
+// A shared-memory descriptor for start address + 16*units: the start address field (bits 0-13)
+// holds addr >> 4 and every shared address is below 256 KB, so the add never carries out of it
+// and only the low word changes (one 32-bit add per MMA instead of rebuilding the descriptor).
+PKV_DEVINLINE uint64_t desc_add(uint64_t d, uint32_t units) {
+  const uint32_t lo = (uint32_t)d + units, hi = (uint32_t)(d >> 32);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16, uint32_t b_mn_major) {
   return (1u << 4)                 // D format: f32
          | (ab_bf16 << 7)          // A format

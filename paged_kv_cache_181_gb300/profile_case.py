@@ -24,16 +24,18 @@ def main() -> None:
     ap.add_argument("--layers", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--fused", action="store_true", help="paged_kv_write_attn instead of the two calls")
     args = ap.parse_args()
     w = configs.ALL[args.workload]
     case = workload.build_case(w, device="cuda", layers=args.layers, data_device="cuda")
     for _ in range(args.steps):
-        case.step(flags=args.flags)
+        case.step(flags=args.flags, fused=args.fused)
     torch.cuda.synchronize()
     bits = _lib.check()
     if bits:
         raise SystemExit(f"device error word 0x{bits:x}")
-    print(f"profile_case: {w.name}, {args.layers} layer(s), {args.steps} forward(s): ok")
+    api = "fused" if args.fused else "two calls"
+    print(f"profile_case: {w.name}, {args.layers} layer(s), {args.steps} forward(s), {api}: ok")
 
 
 if __name__ == "__main__":
