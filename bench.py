@@ -335,6 +335,9 @@ def run_ours(args, world, rank, local):
 
     traffic = read_traffic(w.name)
 
+    # The same step captured once in a CUDA graph and replayed.
+    graph = measure_graph(case, args.steps, fused, ms_step) if not args.no_graph else None
+
     # The other way to run the same forward (two calls per layer, or the fused call).
     alt = measure_alt_step(case, stream, args.steps, ms_step, not fused) if not args.no_alt else None
 
@@ -371,6 +374,8 @@ def run_ours(args, world, rank, local):
         result["e2e"] = e2e
     if kv_layout is not None:
         result["kv_layout"] = kv_layout
+    if graph is not None:
+        result["graph"] = graph
     if alt is not None:
         result["fused" if not fused else "two_call"] = alt
     if packed_rows is not None:
@@ -381,7 +386,37 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v6-fused"
+KERNEL_REV = "tc-v7-sched"
+
+
+def measure_graph(case, steps: int, fused: bool, main_ms_step: float) -> dict:
+    """The forward step captured in a CUDA graph (every layer's launches) and replayed ``steps`` times."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        case.step(fused=fused)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        case.step(fused=fused)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * case.layers
+    del g
+    return {"ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "main_step_ms": main_ms_step, "note": "same step, all launches replayed from one CUDA graph"}
 
 
 def measure_alt_step(case, stream, steps: int, main_ms_step: float, fused: bool) -> dict:
@@ -600,6 +635,7 @@ def main():
     ap.add_argument("--two-call", action="store_true",
                     help="time the forward as paged_kv_write + paged_attn_varlen per layer (default: the fused call)")
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other API for comparison")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
