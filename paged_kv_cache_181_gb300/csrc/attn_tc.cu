@@ -96,16 +96,6 @@ struct TcMaps {
   CUtensorMap kn1, vn1;  //   the same, box = 64 columns of one token
 };
 
-// Work items (one CTA each, in launch order): pairs of 128-query tiles of one (row, query head),
-// then single tiles -- the last `split` pairs broken in two, and each (row, head)'s odd last tile.
-// Blocks start in index order as SMs free up, so the cheaper single-tile CTAs fill the last wave.
-struct TcSched {
-  int n_t;     // query tiles per (row, head): ceil(max_query_len / 128)
-  int np;      // tile pairs per (row, head): n_t / 2
-  int pairs;   // B * Hq * np
-  int split;   // trailing pairs issued as two single-tile items
-};
-
 // The maps one operand (K or V) is loaded through.
 struct OperandMaps {
   const CUtensorMap *blk, *tile, *row, *new5, *new8, *new1;
@@ -215,37 +205,25 @@ PKV_DEVINLINE void fused_write_share(const PkvAttnArgs& a, int warp, int lane) {
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ TcMaps maps, const PkvAttnArgs a, const TcSched sc) {
+    attn_tc_kernel(const __grid_constant__ TcMaps maps, const PkvAttnArgs a) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = a.Hq / a.Hkv;
-  // Decode the work item: (row b, kv head, group member gi, first tile t0, tiles nt).
-  int gi, kvh, b, t0, nt;
-  {
-    const int item = blockIdx.x;
-    const int direct = sc.pairs - sc.split;
-    int u, p = 0;
-    if (item < direct + 2 * sc.split) {  // a pair, or half of a split pair
-      u = item < direct ? item : direct + ((item - direct) >> 1);
-      gi = u % g;
-      u /= g;
-      p = u % sc.np;
-      u /= sc.np;
-      t0 = 2 * p + (item < direct ? 0 : ((item - direct) & 1));
-      nt = item < direct ? 2 : 1;
-    } else {  // the odd last tile of a (row, head)
-      u = item - direct - 2 * sc.split;
-      gi = u % g;
-      u /= g;
-      t0 = sc.n_t - 1;
-      nt = 1;
-    }
-    kvh = u % a.Hkv;
-    b = u / a.Hkv;
-  }
+  // CTA -> (group member gi, tile pair, kv head, row): the CTAs of one (row, kv head) are
+  // adjacent in launch order, so they run together and share its keys and values in L2.
+  // (Issuing the odd last tiles of every head after all pairs, to fill the last wave with
+  // cheaper CTAs, gained 1 % and doubled the DRAM reads: those tiles re-read evicted keys.)
+  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
+  int u = blockIdx.x;
+  const int gi = u % g;
+  u /= g;
+  const int t0 = 2 * (u % n_qp);
+  u /= n_qp;
+  const int kvh = u % a.Hkv;
+  const int b = u / a.Hkv;
   const int h = kvh * g + gi;
   const int split = blockIdx.y;
 
@@ -275,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fused_write_share(a, warp, lane);
     return;
   }
-  const int n_q = nt == 2 && i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
+  const int n_q = i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -720,23 +698,11 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
     attr_set[dev] = true;
   }
   const int g = a.Hq / a.Hkv;
-  const int64_t heads = (int64_t)a.B * a.Hq;
-  TcSched sc{};
-  sc.n_t = (a.max_query_len + BM - 1) / BM;
-  sc.np = sc.n_t / 2;
-  const int64_t pairs = heads * sc.np, odd = heads * (sc.n_t & 1);
-  if (pairs + odd > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
-  sc.pairs = (int)pairs;
-  // Break the pairs left over after the last full wave into single tiles when those and the odd
-  // tiles fit in one wave: a single-tile CTA takes about 0.6 of a pair's time (it still streams
-  // every key), so the last wave ends sooner.
-  int sms = pkv_sm_count();
-  if (sms <= 0) sms = 152;
-  const int64_t rem = pairs % sms;
-  sc.split = (a.num_splits == 1 && rem > 0 && 2 * rem + odd <= sms) ? (int)rem : 0;
-  const int64_t ctas = pairs + sc.split + odd;
+  const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
+  const int64_t ctas = (int64_t)a.B * a.Hkv * n_qp * g;
+  if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)ctas, (unsigned)a.num_splits);
-  attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a, sc);
+  attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a);
   return (int)cudaGetLastError();
 }
 
