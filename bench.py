@@ -353,6 +353,7 @@ def run_ours(args, world, rank, local):
 
     # Packed heterogeneous rows: one call over rows of different shapes and query offsets.
     packed_rows = measure_packed(stream, peaks) if not args.no_packed else None
+    split_kv = measure_split_kv(stream, peaks) if not args.no_packed else None
 
     # e2e: inputs from pinned host memory every step, outputs back to the host.
     e2e = run_e2e(case, args, world, stream, fused) if not args.no_e2e else None
@@ -388,6 +389,8 @@ def run_ours(args, world, rank, local):
         result["fused" if not fused else "two_call"] = alt
     if packed_rows is not None:
         result["packed_rows"] = packed_rows
+    if split_kv is not None:
+        result["split_kv"] = split_kv
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = {k: v for k, v in cpu_oracle_sample(w).items() if k != "seconds"}
     if rank == 0:
@@ -447,6 +450,41 @@ def measure_alt_step(case, stream, steps: int, main_ms_step: float, fused: bool)
             "main_step_ms": main_ms_step, "main_over_this": main_ms_step / ms}
 
 
+def _time_packed(pc, stream, flags: int, reps: int) -> float:
+    import torch
+
+    for _ in range(3):
+        pc.attend(flags=flags, stream=stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        pc.attend(flags=flags, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+
+def measure_split_kv(stream, peaks: dict, reps: int = 20) -> dict:
+    """Split-KV + combine where it matters: few (row, head) units over a long window."""
+    import torch
+
+    from paged_kv_cache_181_gb300 import _lib, configs, packed
+
+    pb = configs.PACKED_FEW_HEADS
+    pc = packed.build_packed(pb, poison=False)
+    flops = 4 * pb.head_dim * pb.num_heads * pairs_from_segments(pc.qsl_host, pc.seq_lens_host, pc.segments)
+    ms_auto = _time_packed(pc, stream, 0, reps)
+    launches = _lib.last_launches()
+    ms_one = _time_packed(pc, stream, _lib.PKV_NO_SPLIT, reps)
+    res = {"workload": pb.name, "ms_split": ms_auto, "ms_no_split": ms_one, "speedup": ms_one / ms_auto,
+           "launches_split": launches, "tflops_split": flops / (ms_auto * 1e-3) / 1e12,
+           "tflops_no_split": flops / (ms_one * 1e-3) / 1e12}
+    del pc
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_packed(stream, peaks: dict, reps: int = 10) -> dict:
     """TFLOP/s of one attention call over the packed heterogeneous rows (6 rows of the 832x480 model)."""
     import torch
@@ -456,16 +494,7 @@ def measure_packed(stream, peaks: dict, reps: int = 10) -> dict:
     pb = configs.PACKED_MIXED
     pc = packed.build_packed(pb, poison=False)
     flops = 4 * pb.head_dim * pb.num_heads * pairs_from_segments(pc.qsl_host, pc.seq_lens_host, pc.segments)
-    for _ in range(3):
-        pc.attend(stream=stream)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
-    for e0, e1 in ev:
-        e0.record(stream)
-        pc.attend(stream=stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    ms = _time_packed(pc, stream, 0, reps)
     tflops = flops / (ms * 1e-3) / 1e12
     res = {"workload": pb.name, "rows": len(pb.rows), "ms_per_launch": ms, "algorithmic_flops_per_launch": flops,
            "achieved": tflops, "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],

@@ -158,4 +158,13 @@ PACKED_MIXED = PackedBatch(
           "actions, mid-sequence re-run, causal, ragged tail",
 )
 
-PACKED = {p.name: p for p in (PACKED_SMALL, PACKED_MIXED)}
+# Few CTAs over a long window: one branch, 8 heads, a 256-token chunk attending 26520 keys -- 8 query-tile
+# pairs for 152 SMs unless the key range is split (split-KV + combine).
+PACKED_FEW_HEADS = PackedBatch(
+    name="few-heads-long-window-bf16", dtype="bf16", num_heads=8, num_kv_heads=8, head_dim=128, block_size=16,
+    pool_blocks=1700, sigma=1.0, seed=35,
+    rows=(PackedRow(256, 26520, 26264, ((26264, 26520),)),),
+    notes="1 row x 8 heads x 256 queries over 26520 keys: needs split-KV to fill the GPU",
+)
+
+PACKED = {p.name: p for p in (PACKED_SMALL, PACKED_MIXED, PACKED_FEW_HEADS)}
