@@ -88,8 +88,9 @@ extern "C" pkv_status paged_kv_write(const void* k, const void* v, const int64_t
                     (long long)row_bytes);
   if (row_bytes / 16 > (1 << 30)) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_kv_write: row too large");
   const int check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
-  unsigned int* err = check ? pkv_device_error_word() : nullptr;
-  if (check && !err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: device error word unavailable");
+  // The error word is always passed: the staged copy reports wait timeouts through it.
+  unsigned int* err = pkv_device_error_word();
+  if (!err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: device error word unavailable");
   const int rc = pkv_launch_kv_write(k, v, slot_mapping, T, key_pool, value_pool, num_slots, (int)row_bytes, err,
                                      check, stream);
   if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
