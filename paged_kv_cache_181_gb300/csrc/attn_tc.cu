@@ -23,12 +23,19 @@
 //              K-major and MN-major shared-memory descriptors need).  Key and
 //              value tiles share one ring of slots (K_j, V_j, K_j+1, ...); a
 //              partly written last block is loaded row by row; value rows past
-//              the last visible key are zeroed;
+//              the last visible key are zeroed.  Contiguous K/V (a consecutive
+//              table): a whole 128-key tile is one box.  Fused write + attention:
+//              the keys at the queries' own positions come from the new k/v
+//              (one box per 16 tokens starting on an 8-token boundary);
 //   warp 1     MMA issuer (one thread) and TMEM owner.  Per key tile j:
 //                P0.V_j -> O0, Q0.K_j+1 -> S0, P1.V_j -> O1, Q1.K_j+1 -> S1
 //              (A = Q from shared memory, or P from TMEM; B = K K-major or V
 //              MN-major from shared memory), so while one softmax group works
-//              on its scores the tensor core runs the other group's MMAs;
+//              on its scores the tensor core runs the other group's MMAs.  An
+//              MMA issue returns when the pipe takes it, so the issue code is
+//              kept lean (descriptors built once, offset per MMA);
+//   warps 2-3  fused write + attention only: the slot-mapping scatter of the
+//              new k/v (this CTA's share of the rows);
 //   warps 4-7  softmax of query tile 0, warps 8-11 of tile 1: one query row per
 //              thread (TMEM lane = row).  Reads a score row from TMEM, masks,
 //              keeps a running maximum in the exp2 domain, writes bf16/f16
@@ -38,7 +45,7 @@
 //              P.V of the previous tile is always complete by the time a score
 //              tile is ready (the score MMA was issued after it), so the rescale
 //              never waits.
-// Registers: the producer/MMA warpgroup (warps 0-3; 2 and 3 idle) gives up
+// Registers: the producer/MMA warpgroup (warps 0-3) gives up
 // registers to the two softmax warpgroups (setmaxnreg 104 / 200; the launch
 // provides 168 per thread and the host refuses to launch a build with another
 // count, so the split always adds up).
