@@ -74,7 +74,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  * 16-token block.  With PKV_CHECK_BOUNDS a row that breaks the promise is flagged (PKV_DEVERR_BLOCK) and
  * loaded block by block. */
 #define PKV_CONTIGUOUS_KV 0x8u
-/* attention: force n (1..8) key-range splits (needs workspace); 0 = plan automatically */
+/* attention: force n (1..16) key-range splits (needs workspace); 0 = plan automatically */
 #define PKV_SPLITS(n) ((((uint32_t)(n)) & 0xffu) << 8)
 
 /* Segment modes. */
@@ -242,8 +242,11 @@ PKV_API pkv_status paged_kv_gather(const void* key_pool, const void* value_pool,
 
 /*
  * paged_attn_workspace_size -- bytes of workspace paged_attn_varlen may use
- * for a call with these sizes (split-KV partial outputs and log-sum-exps).
- * Tq = total query tokens.  0 means no workspace is ever needed.
+ * for a call with these sizes (split-KV partial outputs and log-sum-exps):
+ * the key-range splits the call would plan for these sizes on the current
+ * device (up to 16, only when one CTA per unit leaves SMs idle), and at least
+ * 8 so that PKV_SPLITS(n <= 8) fits.  Tq = total query tokens; 0 for empty
+ * sizes.  A smaller workspace makes a planned split count shrink to what fits.
  */
 PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len);
 

@@ -25,7 +25,8 @@ int current_device() {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-constexpr int kMaxSplits = 8;
+constexpr int kMaxSplits = 16;
+constexpr int kWorkspaceSplits = 8;  // paged_attn_workspace_size covers at least this many (forced splits)
 
 }  // namespace
 
@@ -137,17 +138,20 @@ namespace {
 // Split the key range only when the grid would otherwise leave SMs idle.
 // `units` = CTAs the unsplit launch has; `tiles` = key tiles per unit.
 int plan_splits(int64_t units, int64_t tiles, int sms, int max_splits) {
-  if (units <= 0 || tiles <= 1) return 1;
+  // Split only when one CTA per unit leaves SMs idle: with a full grid, splits only add each CTA's
+  // fixed cost and the combine (2 splits cost +8 % on the long-window workload).
+  if (units <= 0 || units >= sms || tiles <= 1) return 1;
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= max_splits; ++s) {
     const int64_t per = (tiles + s - 1) / s;
     if (s > 1 && per < 4) break;  // too little work per split
-    const int64_t ctas = units * s;
-    const int64_t waves = (ctas + sms - 1) / sms;
-    // cost model: waves x per-split length, plus a small charge per split for the combine
-    const double cost = (double)waves * (double)(per + 2) + 0.02 * s * (double)tiles;
-    if (cost < best_cost * 0.97) {
+    const int64_t waves = (units * s + sms - 1) / sms;
+    // Cost in key tiles: each wave takes its split's tiles plus a CTA's fixed cost (prologue, epilogue,
+    // partial store: about 8 tiles' time), and the combine about 0.3 tiles per split.  Fit to one row x
+    // 8 heads x 256 queries over 26520 keys: 354 / 193 / 113 / 73 / 61 us for 1 / 2 / 4 / 8 / 16 splits.
+    const double cost = (double)waves * (double)(per + 8) + 0.3 * s;
+    if (cost < best_cost) {
       best_cost = cost;
       best = s;
     }
@@ -157,12 +161,27 @@ int plan_splits(int64_t units, int64_t tiles, int sms, int max_splits) {
 
 }  // namespace
 
+// Key-range splits the call plans from host-visible sizes: only when one CTA per unit would leave
+// SMs idle.  A unit is what one CTA covers: 256 queries of one (row, head) for the tensor-core
+// kernel, 16 for the CUDA-core one.
+static int planned_splits(int B, int Hq, int max_query_len, int max_seq_len, bool tc, int sms) {
+  const int64_t q_unit = tc ? 256 : 16;
+  const int64_t k_tile = tc ? 128 : 32;
+  const int64_t units = (int64_t)B * Hq * ((max_query_len + q_unit - 1) / q_unit);
+  const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
+  return plan_splits(units, tiles, tc ? sms : sms * 8, kMaxSplits);
+}
+
 extern "C" size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len) {
-  (void)B;
-  (void)max_query_len;
-  (void)max_seq_len;
   if (Tq <= 0 || Hq <= 0 || D <= 0) return 0;
-  return (size_t)kMaxSplits * (size_t)Tq * (size_t)Hq * ((size_t)D + 1) * sizeof(float);
+  int sms = pkv_sm_count();
+  if (sms <= 0) sms = 152;
+  int splits = kWorkspaceSplits;
+  for (int tc = 0; tc < 2; ++tc) {
+    const int s = planned_splits(B, Hq, max_query_len, max_seq_len, tc == 1, sms);
+    splits = s > splits ? s : splits;
+  }
+  return (size_t)splits * (size_t)Tq * (size_t)Hq * ((size_t)D + 1) * sizeof(float);
 }
 
 namespace {
@@ -239,11 +258,11 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
   if (forced > 0) {
     splits = forced > kMaxSplits ? kMaxSplits : forced;
   } else if (!(flags & PKV_NO_SPLIT) && workspace && ws_bytes) {
-    const int64_t q_tile = use_tc ? 128 : 16;
-    const int64_t k_tile = use_tc ? 128 : 32;
-    const int64_t units = (int64_t)B * Hq * ((max_query_len + q_tile - 1) / q_tile);
-    const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
-    splits = plan_splits(units, tiles, use_tc ? sms : sms * 8, kMaxSplits);
+    splits = planned_splits(B, Hq, max_query_len, max_seq_len, use_tc, sms);
+    // A planned split count the workspace cannot hold shrinks to what it can.
+    const size_t per_split = (size_t)Tq * Hq * ((size_t)D + 1) * sizeof(float);
+    const size_t fits = per_split ? ws_bytes / per_split : 0;
+    if ((size_t)splits > fits) splits = fits > 1 ? (int)fits : 1;
   }
   if (splits > 1) {
     const size_t need = (size_t)splits * (size_t)Tq * Hq * ((size_t)D + 1) * sizeof(float);

@@ -25,11 +25,29 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--fused", action="store_true", help="paged_kv_write_attn instead of the two calls")
+    ap.add_argument("--packed", default=None, help="run this packed batch's attention call instead (configs.PACKED)")
+    ap.add_argument("--gather", action="store_true", help="also stage each layer's window (paged_kv_gather)")
     args = ap.parse_args()
+    if args.packed:
+        from . import packed
+
+        pc = packed.build_packed(configs.PACKED[args.packed], poison=False)
+        for _ in range(args.steps):
+            pc.attend(flags=args.flags)
+        torch.cuda.synchronize()
+        bits = _lib.check()
+        if bits:
+            raise SystemExit(f"device error word 0x{bits:x}")
+        print(f"profile_case: {args.packed}, {args.steps} attention call(s): ok")
+        return
     w = configs.ALL[args.workload]
     case = workload.build_case(w, device="cuda", layers=args.layers, data_device="cuda")
+    st = case.make_staging() if args.gather else None
     for _ in range(args.steps):
         case.step(flags=args.flags, fused=args.fused)
+        if st is not None:
+            for layer in range(case.layers):
+                case.stage(layer, st)
     torch.cuda.synchronize()
     bits = _lib.check()
     if bits:
