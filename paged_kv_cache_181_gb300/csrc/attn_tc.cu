@@ -56,6 +56,7 @@
 
 #include <cuda.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -691,10 +692,12 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
     }
   }
   const size_t smem = sizeof(TcSmem<D>) + 1024;
-  static bool attr_set[64] = {};
+  // Per device, once; racing first calls from several host threads only repeat the same settings.
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  const bool cached = dev >= 0 && dev < 64;
+  if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
     // The warpgroup register split is only valid for the register count it was sized for.
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, BF16>);
@@ -702,7 +705,7 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
     if (fa.numRegs != kLaunchRegs) return (int)cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(attn_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    attr_set[dev] = true;
+    if (cached) attr_set[dev].store(true, std::memory_order_release);
   }
   const int g = a.Hq / a.Hkv;
   const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);

@@ -13,6 +13,8 @@
 // bandwidth), against 25.3 us for one warp per row with 8 16-byte loads in
 // flight per lane -- which stays as the kernel for rows too wide to stage.
 
+#include <atomic>
+
 #include "kv_copy.cuh"
 #include "tc_ptx.cuh"
 
@@ -109,14 +111,16 @@ int pkv_launch_kv_write(const void* k, const void* v, const int64_t* slots, int6
   if (sms <= 0) sms = 152;
   const int64_t smem = (int64_t)kStages * row_bytes;
   if (smem <= kMaxStageBytes && err) {
-    static int set_for[64] = {};
+    // Per device, once; racing first calls from several host threads only repeat the same setting.
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && smem > set_for[dev]) {
+    const bool cached = dev >= 0 && dev < 64;
+    if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
       const cudaError_t e = cudaFuncSetAttribute(kv_write_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  kMaxStageBytes);
       if (e != cudaSuccess) return (int)e;
-      set_for[dev] = kMaxStageBytes;
+      if (cached) attr_set[dev].store(true, std::memory_order_release);
     }
     int64_t grid = (2 * T + kStages - 1) / kStages;
     const int64_t cap = (int64_t)sms * kCtasPerSm;

@@ -91,72 +91,8 @@ PKV_DEVINLINE void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int 
       : "memory");
 }
 
-// Multicast variants: the box lands at the same shared-memory offset in every CTA
-// of `mask` (within this cluster) and completes bytes on the same-offset mbarrier there.
-PKV_DEVINLINE void tma_load_5d_mc(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4, uint64_t* bar,
-                                  uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-PKV_DEVINLINE void tma_load_3d_mc(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-
-PKV_DEVINLINE uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster arrives and waits (release / acquire).
-PKV_DEVINLINE void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of this cluster.
-PKV_DEVINLINE uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-
-PKV_DEVINLINE int ld_cluster_s32(uint32_t cluster_addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
-// Arrive on an mbarrier given by its shared::cluster address (possibly in another CTA).
-PKV_DEVINLINE void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 PKV_DEVINLINE void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
-// ---------------------------------------------------------------- cp.async (16-byte, L2 only)
-
-// Copy 16 bytes global -> shared; with src_bytes == 0 nothing is read and the 16 bytes are zero-filled.
-PKV_DEVINLINE void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// Arrive on `bar` once every cp.async this thread issued so far has landed (count not incremented).
-PKV_DEVINLINE void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -170,40 +106,6 @@ PKV_DEVINLINE void tmem_alloc(uint32_t* dst, uint32_t ncols) {
 PKV_DEVINLINE void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
 PKV_DEVINLINE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// ---- CTA-pair (cta_group::2) forms: every tcgen05 instruction of a kernel uses one cta_group.
-// Allocation and deallocation are performed collectively by one warp in each CTA of the pair.
-PKV_DEVINLINE void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-               : "memory");
-}
-PKV_DEVINLINE void tmem_relinquish2() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory"); }
-PKV_DEVINLINE void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Pair MMA issued by one thread of the even CTA: M = 256 rows, rows 0-127 (A and D) in the even
-// CTA's TMEM and rows 128-255 in the odd CTA's, at the same addresses; B's N columns split in
-// halves, each held at the same shared-memory offset in one CTA.
-PKV_DEVINLINE void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on the same-offset mbarrier of every CTA in `mask` once the pair MMAs issued so far are done.
-PKV_DEVINLINE void mma_commit2_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]   (kind::f16, fp32 accumulate)
@@ -234,15 +136,6 @@ PKV_DEVINLINE void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uin
 PKV_DEVINLINE void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
-}
-
-// Same, arriving on the same-offset mbarrier in every CTA of `mask`.
-PKV_DEVINLINE void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 PKV_DEVINLINE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
