@@ -341,6 +341,15 @@ PKV_API int pkv_last_launches(void);
  */
 PKV_API int pkv_sm_count(void);
 
+/*
+ * pkv_selftest_wait -- run the kernels' bounded pipeline wait on its own: one CTA waits on an
+ * mbarrier that nothing completes, for limit_ns of wall time (0 < limit_ns <= 10 s), then sets
+ * PKV_DEVERR_TIMEOUT in the device error word and exits.  A diagnostic (no counterpart on the
+ * pages): it shows that an expired wait reports through pkv_check and leaves the context usable.
+ * Asynchronous on `stream`.  Errors: PKV_ERR_INVALID_ARG (limit), PKV_ERR_CUDA (launch).
+ */
+PKV_API pkv_status pkv_selftest_wait(uint64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
     "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
     "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches", "paged_attn_varlen_noalloc",
-    "paged_kv_gather", "paged_kv_write_attn",
+    "paged_kv_gather", "paged_kv_write_attn", "pkv_selftest_wait",
 )
 
 
@@ -73,6 +73,7 @@ def _load() -> C.CDLL:
         "paged_kv_write_attn": (C.c_int, [vp, vp, vp, vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int,
                                           C.c_int, C.c_int, vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float,
                                           vp, vp, vp, vp, C.c_size_t, C.c_uint32, vp]),
+        "pkv_selftest_wait": (C.c_int, [C.c_uint64, vp]),
         "paged_kv_gather": (C.c_int, [vp, vp, C.c_int64, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, C.c_int64,
                                       C.c_int, C.c_int, C.c_int, C.c_uint32, vp]),
         "paged_attn_workspace_size": (C.c_size_t, [C.c_int64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
@@ -314,6 +315,11 @@ def check(stream=None) -> int:
     if st not in (PKV_OK, PKV_ERR_DEVICE_CHECK):
         _ok(st)
     return int(bits.value)
+
+
+def selftest_wait(limit_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (see include/pagedkv.h); read the result with check()."""
+    _ok(lib.pkv_selftest_wait(int(limit_ns), _stream(stream)))
 
 
 def last_launches() -> int:

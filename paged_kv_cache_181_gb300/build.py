@@ -24,7 +24,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["device.cu", "kv_write.cu", "attn_simt.cu", "attn_tc.cu", "noalloc.cu"]
+CUDA_SOURCES = ["device.cu", "kv_write.cu", "attn_simt.cu", "attn_tc.cu", "noalloc.cu", "selftest.cu"]
 HOST_SOURCES = ["host.cpp"]
 
 

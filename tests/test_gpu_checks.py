@@ -118,3 +118,29 @@ def test_long_window_forty_layers_full_size(lib):
         want = cases.expected(w, oc, sample)
         max_abs, mean_abs = cases.compare(case.out[layer].float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
         assert max_abs <= 2e-2 and mean_abs <= 2e-3, (layer, max_abs, mean_abs)
+
+
+def test_expired_wait_reports_timeout_and_leaves_the_context_usable(lib):
+    # The kernels' bounded pipeline wait, made to run out on a barrier nothing completes.
+    import time
+
+    from paged_kv_cache_181_gb300 import workload
+
+    t0 = time.perf_counter()
+    lib.selftest_wait(50_000_000)  # 50 ms
+    bits = lib.check()
+    elapsed = time.perf_counter() - t0
+    assert bits & lib.PKV_DEVERR_TIMEOUT
+    assert 0.04 < elapsed < 5.0
+    assert lib.check() == 0  # check() cleared the word
+    # The context still works: a normal call runs and matches the oracle.
+    w = configs.TINY
+    case = workload.build_case(w, poison=True, keep_draws=True, layers=1)
+    case.write(0)
+    out = case.attend(0)
+    torch.cuda.synchronize()
+    assert lib.check() == 0
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, case.draws[0], oc)
+    max_abs, _ = cases.compare(out.float().cpu().numpy(), cases.expected(w, oc), w.dtype)
+    assert max_abs <= cases.TOL[w.dtype][0]
