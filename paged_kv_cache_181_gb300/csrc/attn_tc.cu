@@ -505,15 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c) s[c] = c < nvis ? s[c] : -INFINITY;
       }
       // Row maximum: four chains of three-input maxima.
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < BN; c += 8) {
-        mx0 = ptx::max3(mx0, s[c], s[c + 1]);
-        mx1 = ptx::max3(mx1, s[c + 2], s[c + 3]);
-        mx2 = ptx::max3(mx2, s[c + 4], s[c + 5]);
-        mx3 = ptx::max3(mx3, s[c + 6], s[c + 7]);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+#pragma unroll
+      for (int c = 16; c < BN; c += 16)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = ptx::max3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       // TMEM loads/stores are warp-collective: the warp rescales together when any
       // of its rows needs it (alpha = 1 for the others).  P.V of tile j-1 is complete:
       // the score MMA of tile j, whose completion was just observed, was issued after it.
@@ -540,12 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P occupies columns [0, BN/2) of the score buffer: 32 scores -> 16 packed columns.
       // Exponent arguments and partial sums run as packed fp32 pairs.
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[16];
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t r[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           float x0, x1;
-          ptx::fma2(x0, x1, s[c * 32 + 2 * e], s[c * 32 + 2 * e + 1], sl2, sl2, -mu, -mu);
+          ptx::fma2(x0, x1, s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1], sl2, sl2, -mu, -mu);
           const float p0 = ptx::ex2(x0);
           const float p1 = ptx::ex2(x1);
           if (e & 1)
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::add2(l0, l1, p0, p1);
           r[e] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
         }
-        ptx::tmem_st16(tmem + lane_base + S_COL + c * 16, r);
+        ptx::tmem_st32(tmem + lane_base + S_COL + c * 32, r);
       }
       l += (l0 + l1) + (l2 + l3);
       ptx::tmem_wait_st();
