@@ -87,8 +87,10 @@ def test_empty_row_and_ragged_batch_match_oracle(lib):
         assert np.abs(out.float().cpu().numpy() - want).max() <= tol
 
 
-def test_long_window_forty_layers_full_size(lib):
-    """The benchmarked workload in its benchmarked launch configuration: 40 layers, one forward.
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two-call"])
+def test_long_window_forty_layers_full_size(lib, fused):
+    """The benchmarked workload in its benchmarked launch configuration: 40 layers, one forward
+    (the fused write + attention call per layer, as bench.py times it, and the two-call form).
 
     Each checked layer is compared on sampled query rows against the float64
     oracle over all 26520 keys; the write is checked bit-exactly at every
@@ -98,7 +100,7 @@ def test_long_window_forty_layers_full_size(lib):
 
     w = configs.LONG_WINDOW
     case = workload.build_case(w, device="cuda", poison=False)
-    case.step()
+    case.step(fused=fused)
     torch.cuda.synchronize()
     assert lib.check() == 0
     oc0 = cases.oracle_metadata(w)
