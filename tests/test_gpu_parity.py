@@ -117,3 +117,34 @@ def test_edge_cases(lib, w):
     max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype)
     tol_max, tol_mean = cases.TOL[w.dtype]
     assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
+
+
+MEDIUM = [
+    # D=64 (10-slot ring, many wraps), GQA 2, one-frame geometry
+    dataclasses.replace(configs.ONE_FRAME, name="one-frame-d64-bf16", head_dim=64, num_heads=12, num_kv_heads=6,
+                        seed=41),
+    # fp16 end to end on the one-frame geometry
+    dataclasses.replace(configs.ONE_FRAME, name="one-frame-f16", dtype="f16", seed=42),
+]
+
+
+@pytest.mark.parametrize("w", MEDIUM, ids=lambda w: w.name)
+@pytest.mark.parametrize("fused", [False, True], ids=["two-call", "fused"])
+def test_medium_workloads_sampled_parity(lib, w, fused):
+    from paged_kv_cache_181_gb300 import workload
+
+    case = workload.build_case(w, poison=True, keep_draws=True, layers=1)
+    if fused:
+        out = case.write_attend(0, flags=lib.PKV_CHECK_BOUNDS)
+    else:
+        case.write(0, lib.PKV_CHECK_BOUNDS)
+        out = case.attend(0, lib.PKV_CHECK_BOUNDS)
+    torch.cuda.synchronize()
+    assert lib.check() == 0
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, case.draws[0], oc)
+    sample = cases.sample_rows(w, 24)
+    want = cases.expected(w, oc, sample)
+    max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
