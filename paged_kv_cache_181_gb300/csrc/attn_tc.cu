@@ -102,6 +102,7 @@ struct TcMaps {
   CUtensorMap kn5, vn5;  // fused call: new tokens in the pool's 5-D view, box = 16 tokens (8-aligned start)
   CUtensorMap kn8, vn8;  //   (D, Hkv, Tq), box = 64 columns x 8 tokens (one atom)
   CUtensorMap kn1, vn1;  //   the same, box = 64 columns of one token
+  CUtensorMap o;         // output (D, Hq, Tq), box = 64 columns x 128 tokens of one head (one-split calls)
 };
 
 // The maps one operand (K or V) is loaded through.
@@ -278,6 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.lim_max = 0;
     sm.abort = 0;
     ptx::fence_mbar_init();
+    // Q does not depend on the key range: its load starts before the rows' key limits are reduced.
+    ptx::mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(n_q * BM * D * 2));
+    for (int t = 0; t < n_q; ++t)
+#pragma unroll
+      for (int dh = 0; dh < D / 64; ++dh)  // rows past the last token read as zeros
+        ptx::tma_load_3d(sm.q[t] + dh * (BM * 128), &maps.q, dh * 64, h, q0 + i0 + t * BM, &sm.q_full);
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&maps.kb);
@@ -351,15 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const OperandMaps km{&maps.kb, &maps.kc, &maps.k1, &maps.kn5, &maps.kn8, &maps.kn1};
     const OperandMaps vm{&maps.vb, &maps.vc, &maps.v1, &maps.vn5, &maps.vn8, &maps.vn1};
-    if (n > 0) {
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(n_q * BM * D * 2));
-        for (int t = 0; t < n_q; ++t)
-#pragma unroll
-          for (int dh = 0; dh < D / 64; ++dh)  // rows past the last token read as zeros
-            ptx::tma_load_3d(sm.q[t] + dh * (BM * 128), &maps.q, dh * 64, h, q0 + i0 + t * BM, &sm.q_full);
-      }
-      __syncwarp();
+    if (n == 0 && lane == 0) {
+      // No key tile to process: nothing will wait for Q, but its copy must land before the CTA exits.
+      int never = 0;
+      ptx::mbar_wait(&sm.q_full, 0, &never, kWaitLimitNs);
     }
     for (int idx = 0; idx < 2 * n; ++idx) {
       if (__any_sync(0xffffffffu, sm.abort != 0)) break;
@@ -564,8 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) note_abort(sm, a.err);
 
     // ---------------------------------------------------------------- epilogue
+    // A full query tile of a one-split call leaves through shared memory (the Q buffer, free once
+    // every MMA is done) and TMA stores: one head's rows are Hq*D apart in the output, so rows
+    // stored thread by thread scatter.  The other tiles store per thread.  `staged` is the same
+    // for every thread of the warpgroup, which meets at a named barrier.
+    const bool staged = a.num_splits == 1 && n > 0 && i0 + grp * BM + BM <= Sq;
+    float o[D];
+    float inv = 0.f;
     if (ok) {
-      float o[D];
       if (n > 0) {
         // mma_done completes exactly once, after every MMA of the CTA.
         if (__all_sync(0xffffffffu, ptx::mbar_wait(&sm.mma_done, 0, &sm.abort, kWaitLimitNs))) {
@@ -584,7 +592,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           l = 0.f;
         }
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      inv = l > 0.f ? 1.f / l : 0.f;
+    }
+    if (staged) {
+      uint8_t* tile = sm.q[grp];  // [D/64][128 rows][128 B], 128-byte swizzled like the Q load
+      if (ok) {
+#pragma unroll
+        for (int dh = 0; dh < D / 64; ++dh)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = o[dh * 64 + k * 8 + 2 * e] * inv;
+              const float x1 = o[dh * 64 + k * 8 + 2 * e + 1] * inv;
+              w[e] = BF16 ? ptx::pack_bf16x2(x0, x1) : ptx::pack_f16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4*>(tile + dh * (BM * 128) + row * 128 + ((k ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+      }
+      ptx::fence_proxy_async_smem();
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(BM) : "memory");
+      if (row == 0 && !sm.abort) {
+#pragma unroll
+        for (int dh = 0; dh < D / 64; ++dh)
+          ptx::tma_store_3d(&maps.o, dh * 64, h, q0 + i0 + grp * BM, tile + dh * (BM * 128));
+        ptx::bulk_commit();
+        ptx::bulk_wait_all();  // done before the CTA (and its shared memory) goes away
+      }
+    } else if (ok) {
       if (!valid) {
         // query row past the end of this row's queries: nothing to store
       } else if (a.num_splits == 1) {
@@ -678,6 +715,7 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
       !encode(&maps.k1, a.k_pool, 3, dims3, str3, box1, BF16) || !encode(&maps.v1, a.v_pool, 3, dims3, str3, box1, BF16) ||
       !encode(&maps.q, a.q, 3, dimsq, strq, boxq, BF16))
     return (int)cudaErrorInvalidValue;
+  if (a.num_splits == 1 && !encode(&maps.o, a.out, 3, dimsq, strq, boxq, BF16)) return (int)cudaErrorInvalidValue;
   if (a.k_new) {
     // New tokens [Tq, Hkv, D]: (D, Hkv, Tq) with the pool's row stride.
     const cuuint64_t dimsn[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)a.Tq};

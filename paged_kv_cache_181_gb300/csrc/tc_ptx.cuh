@@ -91,6 +91,16 @@ PKV_DEVINLINE void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int 
       : "memory");
 }
 
+// 3-D tiled store shared -> global (bulk async-group of this thread); rows outside the tensor are not written.
+PKV_DEVINLINE void tma_store_3d(const void* tmap, int x, int y, int z, const void* src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(z), "r"(smem_u32(src))
+               : "memory");
+}
+PKV_DEVINLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk store this thread committed has completed.
+PKV_DEVINLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 PKV_DEVINLINE void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
