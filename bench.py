@@ -397,7 +397,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v9"
+KERNEL_REV = "tc-v10"
 
 
 def measure_graph(case, steps: int, fused: bool, main_ms_step: float) -> dict:
@@ -640,6 +640,20 @@ def run_e2e(case, args, world, stream, fused: bool):
         ev.record(stream)
     e2e_step()
     torch.cuda.synchronize()
+    # One step's uploads alone, without compute: the host->device bandwidth this machine gives, so that an
+    # upload-bound step shows as such beside the overlapped one.
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(up):
+        u0.record(up)
+        for hd, dd in zip(meta_host, meta_sets[0]):
+            dd.copy_(hd, non_blocking=True)
+        for l in range(layers):
+            case.q[l].copy_(host_q[l], non_blocking=True)
+            case.k_new[l].copy_(host_k[l], non_blocking=True)
+            case.v_new[l].copy_(host_v[l], non_blocking=True)
+        u1.record(up)
+    torch.cuda.synchronize()
+    upload_ms = u0.elapsed_time(u1)
     steps = max(1, min(args.steps, 5))
     barrier(world)
     torch.cuda.synchronize()
@@ -655,7 +669,8 @@ def run_e2e(case, args, world, stream, fused: bool):
     flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * layers * world
     api = "paged_kv_write_attn" if fused else "paged_kv_write + paged_attn_varlen"
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory"}
+            "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
+            "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9}
 
 
 def main():

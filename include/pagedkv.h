@@ -244,9 +244,17 @@ PKV_API pkv_status paged_kv_gather(const void* key_pool, const void* value_pool,
  * paged_attn_workspace_size -- bytes of workspace paged_attn_varlen may use
  * for a call with these sizes (split-KV partial outputs and log-sum-exps):
  * the key-range splits the call would plan for these sizes on the current
- * device (up to 16, only when one CTA per unit leaves SMs idle), and at least
- * 8 so that PKV_SPLITS(n <= 8) fits.  Tq = total query tokens; 0 for empty
- * sizes.  A smaller workspace makes a planned split count shrink to what fits.
+ * device (up to 16; see below), and at least 8 so that PKV_SPLITS(n <= 8)
+ * fits.  Tq = total query tokens; 0 for empty sizes.  A smaller workspace
+ * makes a planned split count shrink to what fits.
+ *
+ * Planning: the tensor-core kernel runs one CTA per item (256 queries of one
+ * row and head).  When the items fill the SMs a whole number of times plus a
+ * partial last wave, the whole waves run unsplit and only the last wave's
+ * items split their key range, into the count that minimises that wave's
+ * estimated time; a second, combine launch merges their partials.  Forced
+ * splits (PKV_SPLITS) split every item.  The CUDA-core kernel splits all of its
+ * items or none.  pkv_last_split_plan reports what the last call chose.
  */
 PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len);
 
@@ -334,6 +342,15 @@ PKV_API pkv_status pkv_check(void* stream, uint32_t* bits);
  * paged_attn_varlen call on this thread launched (0 if it launched nothing).
  */
 PKV_API int pkv_last_launches(void);
+
+/*
+ * pkv_last_split_plan -- the key-range split of the last paged_attn_varlen /
+ * paged_kv_write_attn call on this thread (each pointer may be NULL):
+ *   splits       splits per split item (1: nothing was split)
+ *   whole_items  items run unsplit before the split ones (tensor-core kernel; 0 when
+ *                every item was split or nothing was)
+ */
+PKV_API void pkv_last_split_plan(int* splits, int64_t* whole_items);
 
 /*
  * pkv_sm_count -- number of SMs of the current device (used to size

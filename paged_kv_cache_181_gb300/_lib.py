@@ -31,7 +31,7 @@ EXPORTS = (
     "pkv_last_error", "pkv_version", "build_segments", "pkv_slot_mapping", "pkv_table_width",
     "pkv_visible_window", "pkv_block_table_row", "paged_kv_write", "paged_attn_workspace_size",
     "paged_attn_varlen", "pkv_check", "pkv_sm_count", "pkv_last_launches", "paged_attn_varlen_noalloc",
-    "paged_kv_gather", "paged_kv_write_attn", "pkv_selftest_wait",
+    "paged_kv_gather", "paged_kv_write_attn", "pkv_selftest_wait", "pkv_last_split_plan",
 )
 
 
@@ -83,6 +83,7 @@ def _load() -> C.CDLL:
         "pkv_check": (C.c_int, [vp, C.POINTER(C.c_uint32)]),
         "pkv_sm_count": (C.c_int, []),
         "pkv_last_launches": (C.c_int, []),
+        "pkv_last_split_plan": (None, [C.POINTER(C.c_int), C.POINTER(C.c_int64)]),
         "paged_attn_varlen_noalloc": (C.c_int, [vp, C.c_int64, C.c_int, vp, vp, C.c_int64, C.c_int, C.c_int, C.c_int,
                                                 C.c_int, vp, C.c_int, C.c_int, vp, vp, C.c_int, C.c_int, C.c_float, vp,
                                                 vp, vp, C.c_uint32, vp]),
@@ -325,6 +326,13 @@ def selftest_wait(limit_ns: int, stream=None) -> None:
 def last_launches() -> int:
     """Kernels launched by the last device call on this thread."""
     return int(lib.pkv_last_launches())
+
+
+def last_split_plan() -> tuple[int, int]:
+    """(splits per split item, items run whole before them) of the last attention call on this thread."""
+    s, w = C.c_int(), C.c_int64()
+    lib.pkv_last_split_plan(C.byref(s), C.byref(w))
+    return int(s.value), int(w.value)
 
 
 def sm_count() -> int:

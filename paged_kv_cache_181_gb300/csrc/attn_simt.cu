@@ -221,11 +221,31 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
 // Lane s reads split s's log-sum-exp (at most 32 splits), the maximum and the weight sum are
 // warp reductions, and the partial rows are read 8 splits at a time so their loads are in
 // flight together (reading the splits one after another was latency-bound: 28 us for 17 MB).
+// With a split tail (split_direct > 0) only the split items' rows are combined: warp w takes
+// row wi % rows of tensor-core item split_direct + wi / rows, decoded as the kernel decodes it.
 template <typename T>
 __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
-  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t wi = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (item >= a.Tq * a.Hq) return;
+  int64_t item = wi;  // token * Hq + head
+  if (a.split_direct > 0) {
+    const int rows = a.max_query_len < kTcItemRows ? a.max_query_len : kTcItemRows;
+    const int g = a.Hq / a.Hkv;
+    const int n_qp = (a.max_query_len + kTcItemRows - 1) / kTcItemRows;
+    const int64_t items = (int64_t)a.B * a.Hq * n_qp;
+    const int64_t u = a.split_direct + wi / rows;
+    if (u >= items) return;
+    const PkvTcItem it = pkv_tc_item((int)u, g, n_qp, a.Hkv);
+    const int i = it.qp * kTcItemRows + (int)(wi % rows);
+    const int q0 = a.query_start_loc[it.b];
+    int Sq = a.query_start_loc[it.b + 1] - q0;
+    Sq = Sq < 0 ? 0 : (Sq > a.max_query_len ? a.max_query_len : Sq);
+    const int64_t tok = (int64_t)q0 + i;
+    if (i >= Sq || tok < 0 || tok >= a.Tq) return;
+    item = tok * a.Hq + it.kvh * g + it.gi;
+  } else if (item >= a.Tq * a.Hq) {
+    return;
+  }
   const int S = a.num_splits;
   const int64_t stride = a.Tq * a.Hq;
   const float lse = lane < S ? a.part_lse[(int64_t)lane * stride + item] : -INFINITY;
@@ -287,8 +307,14 @@ int pkv_launch_attn_simt(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
 
 int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  const int64_t threads = a.Tq * a.Hq * 32;
-  const unsigned grid = (unsigned)((threads + 255) / 256);
+  int64_t warps = a.Tq * a.Hq;
+  if (a.split_direct > 0) {
+    const int64_t n_qp = (a.max_query_len + kTcItemRows - 1) / kTcItemRows;
+    const int64_t rows = a.max_query_len < kTcItemRows ? a.max_query_len : kTcItemRows;
+    warps = ((int64_t)a.B * a.Hq * n_qp - a.split_direct) * rows;
+  }
+  if (warps <= 0) return 0;
+  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
   switch (dt) {
     case PKV_F32: attn_combine_kernel<float><<<grid, 256, 0, s>>>(a); break;
     case PKV_BF16: attn_combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a); break;

@@ -8,7 +8,8 @@
 // prefix [0, limit) of its row's keys).
 //
 // One CTA = 256 queries of one (row, query head) -- two 128-query tiles that
-// share every key/value tile -- and one key-range split.  Sharing halves the
+// share every key/value tile -- or, for the items of a last, partly filled
+// wave, one key-range split of them (the combine merges the splits).  Sharing halves the
 // key/value bytes each SM has to take in per FLOP, which is what bounds this
 // workload on this part (a one-tile CTA spent longer receiving its 64 KB per
 // key tile than its tensor core spent on the MMAs).
@@ -67,6 +68,7 @@ namespace {
 
 constexpr int BM = 128;  // queries per tile; two tiles per CTA
 constexpr int BN = 128;  // keys per tile
+static_assert(2 * BM == kTcItemRows, "a work item is one tile pair");
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // registers per thread the kernel is compiled to (checked at launch)
 constexpr int kRegsLow = 104;     // producer / MMA warpgroup
@@ -225,16 +227,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // adjacent in launch order, so they run together and share its keys and values in L2.
   // (Issuing the odd last tiles of every head after all pairs, to fill the last wave with
   // cheaper CTAs, gained 1 % and doubled the DRAM reads: those tiles re-read evicted keys.)
+  // With a split tail, the CTAs past the first `split_direct` items take num_splits each per item:
+  // only the items of the last, partly filled wave are split.
+  // (`whole` and `split` are cheap to recompute from the launch parameters, so the epilogue
+  // does that instead of keeping them live through the softmax loop.)
   const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
-  int u = blockIdx.x;
-  const int gi = u % g;
-  u /= g;
-  const int t0 = 2 * (u % n_qp);
-  u /= n_qp;
-  const int kvh = u % a.Hkv;
-  const int b = u / a.Hkv;
+  const bool whole = a.num_splits == 1 || (int)blockIdx.x < a.split_direct;
+  int u = blockIdx.x, split = 0;
+  if (!whole) {
+    const int p = u - a.split_direct;
+    u = a.split_direct + p / a.num_splits;
+    split = p % a.num_splits;
+  }
+  const int nsplit = whole ? 1 : a.num_splits;
+  const PkvTcItem it = pkv_tc_item(u, g, n_qp, a.Hkv);
+  const int gi = it.gi, t0 = 2 * it.qp, kvh = it.kvh, b = it.b;
   const int h = kvh * g + gi;
-  const int split = blockIdx.y;
 
   const int q0 = a.query_start_loc[b];
   int Sq = a.query_start_loc[b + 1] - q0;
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const int kv_hi = sm.lim_max;
   const int n_tiles = (kv_hi + BN - 1) / BN;
-  const int per = (n_tiles + a.num_splits - 1) / a.num_splits;
+  const int per = (n_tiles + nsplit - 1) / nsplit;
   const int t_begin = split * per;
   const int t_end = min(n_tiles, t_begin + per);
   const int n = t_end > t_begin ? t_end - t_begin : 0;
@@ -570,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA is done) and TMA stores: one head's rows are Hq*D apart in the output, so rows
     // stored thread by thread scatter.  The other tiles store per thread.  `staged` is the same
     // for every thread of the warpgroup, which meets at a named barrier.
-    const bool staged = a.num_splits == 1 && n > 0 && i0 + grp * BM + BM <= Sq;
+    const bool whole_out = a.num_splits == 1 || (int)blockIdx.x < a.split_direct;
+    const bool staged = whole_out && n > 0 && i0 + grp * BM + BM <= Sq;
     float o[D];
     float inv = 0.f;
     if (ok) {
@@ -624,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok) {
       if (!valid) {
         // query row past the end of this row's queries: nothing to store
-      } else if (a.num_splits == 1) {
+      } else if (whole_out) {
         uint4* dst = reinterpret_cast<uint4*>((uint16_t*)a.out + (tok * a.Hq + h) * D);
 #pragma unroll
         for (int v8 = 0; v8 < D / 8; ++v8) {
@@ -638,14 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[v8] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)split * a.Tq + tok) * a.Hq + h) * D);
+        const int sp = ((int)blockIdx.x - a.split_direct) % a.num_splits;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)sp * a.Tq + tok) * a.Hq + h) * D);
 #pragma unroll
         for (int v4 = 0; v4 < D / 4; ++v4) {
           dst[v4] = n > 0 ? make_float4(o[v4 * 4] * inv, o[v4 * 4 + 1] * inv, o[v4 * 4 + 2] * inv, o[v4 * 4 + 3] * inv)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // natural-log log-sum-exp of this split: ln 2 * (m_ref + log2 l)
-        a.part_lse[((int64_t)split * a.Tq + tok) * a.Hq + h] =
+        a.part_lse[((int64_t)sp * a.Tq + tok) * a.Hq + h] =
             (n > 0 && l > 0.f) ? 0.6931471805599453f * (m_ref + __log2f(l)) : -INFINITY;
       }
     }
@@ -715,7 +725,7 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
       !encode(&maps.k1, a.k_pool, 3, dims3, str3, box1, BF16) || !encode(&maps.v1, a.v_pool, 3, dims3, str3, box1, BF16) ||
       !encode(&maps.q, a.q, 3, dimsq, strq, boxq, BF16))
     return (int)cudaErrorInvalidValue;
-  if (a.num_splits == 1 && !encode(&maps.o, a.out, 3, dimsq, strq, boxq, BF16)) return (int)cudaErrorInvalidValue;
+  if ((a.num_splits == 1 || a.split_direct > 0) && !encode(&maps.o, a.out, 3, dimsq, strq, boxq, BF16)) return (int)cudaErrorInvalidValue;
   if (a.k_new) {
     // New tokens [Tq, Hkv, D]: (D, Hkv, Tq) with the pool's row stride.
     const cuuint64_t dimsn[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)a.Tq};
@@ -747,9 +757,11 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   }
   const int g = a.Hq / a.Hkv;
   const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);
-  const int64_t ctas = (int64_t)a.B * a.Hkv * n_qp * g;
+  const int64_t items = (int64_t)a.B * a.Hkv * n_qp * g;
+  if (a.split_direct < 0 || a.split_direct > items) return (int)cudaErrorInvalidValue;
+  const int64_t ctas = a.num_splits > 1 ? a.split_direct + (items - a.split_direct) * a.num_splits : items;
   if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)ctas, (unsigned)a.num_splits);
+  dim3 grid((unsigned)ctas);
   attn_tc_kernel<D, BF16><<<grid, kThreads, smem, s>>>(maps, a);
   return (int)cudaGetLastError();
 }

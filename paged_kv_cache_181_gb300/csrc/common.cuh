@@ -56,3 +56,23 @@ PKV_DEVINLINE int pkv_row_limit(int p, int L, const pkv_segment* segs, int s_beg
   *uncovered = true;
   return 0;
 }
+
+// Work items of the tensor-core kernel: 256 queries (two 128-query tiles) of one (row, head).
+// Item u -> (group member gi, tile pair qp, kv head kvh, row b), gi fastest, so the items of one
+// (row, kv head) are adjacent and run together.  The split-KV combine decodes the same order.
+constexpr int kTcItemRows = 256;
+
+struct PkvTcItem {
+  int gi, qp, kvh, b;
+};
+
+PKV_DEVINLINE PkvTcItem pkv_tc_item(int u, int g, int n_qp, int Hkv) {
+  PkvTcItem it;
+  it.gi = u % g;
+  u /= g;
+  it.qp = u % n_qp;
+  u /= n_qp;
+  it.kvh = u % Hkv;
+  it.b = u / Hkv;
+  return it;
+}

@@ -135,41 +135,54 @@ extern "C" pkv_status paged_kv_gather(const void* key_pool, const void* value_po
 
 namespace {
 
-// Split the key range only when the grid would otherwise leave SMs idle.
-// `units` = CTAs the unsplit launch has; `tiles` = key tiles per unit.
-int plan_splits(int64_t units, int64_t tiles, int sms, int max_splits) {
-  // Split only when one CTA per unit leaves SMs idle: with a full grid, splits only add each CTA's
-  // fixed cost and the combine (2 splits cost +8 % on the long-window workload).
-  if (units <= 0 || units >= sms || tiles <= 1) return 1;
+struct SplitPlan {
+  int splits;      // key-range splits of each split item (1: no split)
+  int64_t direct;  // items run whole before the split ones
+};
+
+// Split the key range only where the grid would otherwise leave SMs idle: the items of the
+// last, partly filled wave.  `items` = CTAs of the unsplit launch, `tiles` = key tiles per item,
+// `sms` = CTAs that run at once.  The `full` whole waves run unsplit; the `tail` items after
+// them split s ways, with s chosen to minimise the tail's time in key tiles: its waves, each
+// taking one split's tiles plus a CTA's fixed cost (prologue, epilogue, partial store: about 8
+// tiles' time), plus the combine at about 0.3 tiles per split.  Fit to one row x 8 heads x 256
+// queries over 26520 keys: 354 / 193 / 113 / 73 / 61 us for 1 / 2 / 4 / 8 / 16 splits.  (Splitting
+// every item of a full grid only adds fixed costs: 2 splits cost +8 % on the long-window workload.)
+SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits, bool tail_ok) {
+  const SplitPlan none{1, items};
+  if (items <= 0 || tiles <= 1 || sms <= 0) return none;
+  const int64_t full = items / sms;
+  const int64_t tail = items - full * sms;
+  if (tail == 0 || (full > 0 && !tail_ok)) return none;
   int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= max_splits; ++s) {
+  double best_cost = (double)(tiles + 8);
+  for (int s = 2; s <= max_splits; ++s) {
     const int64_t per = (tiles + s - 1) / s;
-    if (s > 1 && per < 4) break;  // too little work per split
-    const int64_t waves = (units * s + sms - 1) / sms;
-    // Cost in key tiles: each wave takes its split's tiles plus a CTA's fixed cost (prologue, epilogue,
-    // partial store: about 8 tiles' time), and the combine about 0.3 tiles per split.  Fit to one row x
-    // 8 heads x 256 queries over 26520 keys: 354 / 193 / 113 / 73 / 61 us for 1 / 2 / 4 / 8 / 16 splits.
+    if (per < 4) break;  // too little work per split
+    const int64_t waves = (tail * s + sms - 1) / sms;
     const double cost = (double)waves * (double)(per + 8) + 0.3 * s;
     if (cost < best_cost) {
       best_cost = cost;
       best = s;
     }
   }
-  return best;
+  return best > 1 ? SplitPlan{best, full * sms} : none;
 }
 
 }  // namespace
 
-// Key-range splits the call plans from host-visible sizes: only when one CTA per unit would leave
-// SMs idle.  A unit is what one CTA covers: 256 queries of one (row, head) for the tensor-core
-// kernel, 16 for the CUDA-core one.
-static int planned_splits(int B, int Hq, int max_query_len, int max_seq_len, bool tc, int sms) {
-  const int64_t q_unit = tc ? 256 : 16;
+// Key-range splits the call plans from host-visible sizes.  An item is what one CTA of the
+// unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 16 for the
+// CUDA-core one.  Only the tensor-core kernel splits a tail behind whole items; the CUDA-core
+// kernel splits all of its items or none (only when they leave SMs idle).
+static SplitPlan planned_splits(int B, int Hq, int max_query_len, int max_seq_len, bool tc, int sms) {
+  const int64_t q_unit = tc ? kTcItemRows : 16;
   const int64_t k_tile = tc ? 128 : 32;
-  const int64_t units = (int64_t)B * Hq * ((max_query_len + q_unit - 1) / q_unit);
+  const int64_t items = (int64_t)B * Hq * ((max_query_len + q_unit - 1) / q_unit);
   const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
-  return plan_splits(units, tiles, tc ? sms : sms * 8, kMaxSplits);
+  SplitPlan p = plan_splits(items, tiles, tc ? sms : sms * 8, kMaxSplits, tc);
+  if (!tc) p.direct = 0;
+  return p;
 }
 
 extern "C" size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len) {
@@ -178,7 +191,7 @@ extern "C" size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, in
   if (sms <= 0) sms = 152;
   int splits = kWorkspaceSplits;
   for (int tc = 0; tc < 2; ++tc) {
-    const int s = planned_splits(B, Hq, max_query_len, max_seq_len, tc == 1, sms);
+    const int s = planned_splits(B, Hq, max_query_len, max_seq_len, tc == 1, sms).splits;
     splits = s > splits ? s : splits;
   }
   return (size_t)splits * (size_t)Tq * (size_t)Hq * ((size_t)D + 1) * sizeof(float);
@@ -199,6 +212,7 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
                      void* out, void* workspace, size_t ws_bytes, uint32_t flags, void* stream, const FusedWrite* fw) {
   pkv_clear_error();
   pkv_set_launches(0);
+  pkv_set_split_plan(1, 0);
   if (Tq < 0 || B < 0 || W < 0 || max_query_len < 0 || max_seq_len < 0 || num_blocks < 0)
     return pkv_fail(PKV_ERR_INVALID_ARG, "%s: negative size", fn);
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv)
@@ -248,17 +262,21 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
   a.err = pkv_device_error_word();
   if (!a.err) return pkv_fail(PKV_ERR_CUDA, "%s: device error word unavailable", fn);
 
-  const bool use_tc = !(flags & PKV_FORCE_SIMT) && pkv_attn_tc_supports(dt, D);
+  // (The tensor-core launcher also declines a non-positive scale; plan for the kernel that runs.)
+  const bool use_tc = !(flags & PKV_FORCE_SIMT) && pkv_attn_tc_supports(dt, D) && softmax_scale > 0.f;
   int sms = pkv_sm_count();
   if (sms <= 0) sms = 152;
 
   // Split planning from host-visible sizes only.
   int forced = (int)((flags >> 8) & 0xffu);
   int splits = 1;
+  int64_t direct = 0;
   if (forced > 0) {
     splits = forced > kMaxSplits ? kMaxSplits : forced;
   } else if (!(flags & PKV_NO_SPLIT) && workspace && ws_bytes) {
-    splits = planned_splits(B, Hq, max_query_len, max_seq_len, use_tc, sms);
+    const SplitPlan plan = planned_splits(B, Hq, max_query_len, max_seq_len, use_tc, sms);
+    splits = plan.splits;
+    direct = plan.direct;
     // A planned split count the workspace cannot hold shrinks to what it can.
     const size_t per_split = (size_t)Tq * Hq * ((size_t)D + 1) * sizeof(float);
     const size_t fits = per_split ? ws_bytes / per_split : 0;
@@ -278,6 +296,8 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
     }
   }
   a.num_splits = splits;
+  a.split_direct = splits > 1 ? (int)direct : 0;
+  pkv_set_split_plan(splits, splits > 1 ? direct : (int64_t)0);
   if (fw) {
     if (!fw->k || !fw->v || !fw->slots) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: NULL k, v or slot_mapping", fn);
     if (!aligned16(fw->k) || !aligned16(fw->v))
@@ -290,7 +310,12 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
 
   int rc = -1;
   if (use_tc) rc = pkv_launch_attn_tc(a, dt, stream);
-  if (rc == -1) rc = pkv_launch_attn_simt(a, dt, stream);
+  if (rc == -1) {
+    // The CUDA-core kernel splits every item or none: its combine merges every row.
+    a.split_direct = 0;
+    pkv_set_split_plan(splits, 0);
+    rc = pkv_launch_attn_simt(a, dt, stream);
+  }
   if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString((cudaError_t)rc));
   if (splits > 1) {
     rc = pkv_launch_attn_combine(a, dt, stream);

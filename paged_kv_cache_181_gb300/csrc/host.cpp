@@ -15,6 +15,8 @@
 namespace {
 thread_local char g_last_error[512] = "";
 thread_local int g_last_launches = 0;
+thread_local int g_last_splits = 1;
+thread_local int64_t g_last_whole_items = 0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t gcd64(int64_t a, int64_t b) {
@@ -40,6 +42,16 @@ void pkv_clear_error() { g_last_error[0] = '\0'; }
 void pkv_set_launches(int n) { g_last_launches = n; }
 
 extern "C" int pkv_last_launches(void) { return g_last_launches; }
+
+void pkv_set_split_plan(int splits, int64_t whole_items) {
+  g_last_splits = splits;
+  g_last_whole_items = whole_items;
+}
+
+extern "C" void pkv_last_split_plan(int* splits, int64_t* whole_items) {
+  if (splits) *splits = g_last_splits;
+  if (whole_items) *whole_items = g_last_whole_items;
+}
 
 extern "C" const char* pkv_last_error(void) { return g_last_error; }
 

@@ -10,6 +10,7 @@
 pkv_status pkv_fail(pkv_status code, const char* fmt, ...);
 void pkv_clear_error();
 void pkv_set_launches(int n);
+void pkv_set_split_plan(int splits, int64_t whole_items);
 
 // Device error word of the current device (PKV_DEVERR_* bits); nullptr when unavailable.
 unsigned int* pkv_device_error_word();
@@ -35,6 +36,10 @@ struct PkvAttnArgs {
   int B, W, Hq, Hkv, D;
   int max_query_len, max_seq_len;
   int num_splits;
+  // Tensor-core grid with a split tail (num_splits > 1): items [0, split_direct) run one CTA
+  // each and write `out`; every later item runs num_splits CTAs over parts of its key range
+  // and leaves partials for the combine.  0: every item is split (the CUDA-core kernel).
+  int split_direct;
   int check;
   int contiguous;  // PKV_CONTIGUOUS_KV
   float scale;

@@ -75,8 +75,9 @@ def oracle_pools(w: Workload, d: synth.Draw, oc: OracleCase) -> None:
     oc.k_pool, oc.v_pool, oc.q = kp, vp, to_np(d.q)
 
 
-def expected(w: Workload, oc: OracleCase, sample=None) -> np.ndarray:
-    return pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, w.head_dim ** -0.5,
+def expected(w: Workload, oc: OracleCase, sample=None, scale=None) -> np.ndarray:
+    scale = w.head_dim ** -0.5 if scale is None else scale
+    return pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, scale,
                               w.block_size, oc.segments, sample=sample)
 
 

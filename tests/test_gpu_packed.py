@@ -74,11 +74,14 @@ def test_packed_rows_equal_each_row_alone():
 
 @pytest.mark.parametrize("pb", [configs.PACKED_MIXED, configs.PACKED_FEW_HEADS], ids=lambda p: p.name)
 def test_packed_full_size_sampled_rows(pb):
-    # PACKED_FEW_HEADS has 8 query-tile pairs in all, so the planner splits the key range (split-KV + combine).
+    # PACKED_FEW_HEADS has 8 query-tile pairs in all, so the planner splits every item's key range
+    # (split-KV + combine).
     from paged_kv_cache_181_gb300 import _lib
 
     pc, out = _run(pb)
     if pb is configs.PACKED_FEW_HEADS:
+        splits, whole = _lib.last_split_plan()
+        assert splits > 1 and whole == 0, (splits, whole)
         assert _lib.last_launches() == 2
     op = cases.oracle_packed(pb, pc.draw)
     sample = cases.sample_packed_rows(pb, 6 if len(pb.rows) > 1 else 24)

@@ -148,3 +148,63 @@ def test_medium_workloads_sampled_parity(lib, w, fused):
     max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
     tol_max, tol_mean = cases.TOL[w.dtype]
     assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
+
+
+def _tail_workload():
+    # One more row than fills every SM once: 8 heads x (SMs // 8 + 1) rows of one 224-query item
+    # each, so the launch runs whole items on every SM and splits the last row's 8 over their keys.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return dataclasses.replace(configs.GQA_ACTION, name="tail-split-gqa", batch=sms // 8 + 1, num_heads=8,
+                               num_kv_heads=2, chunk_tokens=208, window_chunks=6, sink_chunks=1,
+                               history_tokens=8 * 208, query_tokens=208, action_len=16, spans=((1248, 1456),),
+                               pool_blocks=4096, seed=51)
+
+
+def _run_tail(lib, w, fused, workspace_splits=None, scale_sign=1.0):
+    from paged_kv_cache_181_gb300 import workload
+
+    case = workload.build_case(w, poison=True, keep_draws=True, layers=1)
+    if workspace_splits is not None:
+        tq = w.batch * w.q_len
+        case.workspace = case.workspace[: workspace_splits * tq * w.num_heads * (w.head_dim + 1) * 4]
+    case.scale *= scale_sign
+    if fused:
+        out = case.write_attend(0, flags=lib.PKV_CHECK_BOUNDS)
+    else:
+        case.write(0, lib.PKV_CHECK_BOUNDS)
+        out = case.attend(0, lib.PKV_CHECK_BOUNDS)
+    launches, plan = lib.last_launches(), lib.last_split_plan()
+    torch.cuda.synchronize()
+    assert lib.check() == 0
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, case.draws[0], oc)
+    want = cases.expected(w, oc, scale=case.scale)
+    max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype)
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
+    return launches, plan
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two-call", "fused"])
+def test_split_tail_parity(lib, fused):
+    """Whole items on every SM plus a key-split tail and its combine: every output against the oracle."""
+    w = _tail_workload()
+    launches, (splits, whole) = _run_tail(lib, w, fused)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert splits > 2 and whole == sms, (splits, whole)
+    assert launches == 2  # attention + combine
+
+
+def test_split_tail_shrinks_to_the_workspace(lib):
+    """A workspace holding two splits' partials: the tail splits in two, the whole items stay whole."""
+    w = _tail_workload()
+    launches, (splits, whole) = _run_tail(lib, w, False, workspace_splits=2)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert splits == 2 and whole == sms and launches == 2, (splits, whole, launches)
+
+
+def test_negative_scale_plans_for_the_kernel_that_runs(lib):
+    """A negative softmax scale runs on the CUDA-core kernel, whose split plan has no whole items."""
+    w = _tail_workload()
+    launches, (splits, whole) = _run_tail(lib, w, False, scale_sign=-1.0)
+    assert whole == 0, (splits, whole)

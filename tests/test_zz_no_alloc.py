@@ -82,6 +82,25 @@ def test_noalloc_matches_workspace_call_on_consecutive_calls(lib):
                 assert err.max() <= 2e-2 and err.mean() <= 2e-3
 
 
+PLANNED = [
+    CASES[0][:8],
+    (4, torch.bfloat16, 8, 8, 64, (256,), (4000,), ([],)),
+    (5, torch.float16, 4, 1, 128, (100, 256, 7), (3000, 2100, 900), ([(1000, 1200)], [], [])),
+]
+
+
+def test_noalloc_planned_splits(lib):
+    # Few items, so the planner splits every item's key range into the scratch; consecutive calls.
+    for _ in range(2):
+        for seed, dtype, hq, hkv, d, sq, kv, spans in PLANNED:
+            c = make_case(seed, dtype, hq, hkv, d, sq, kv, spans)
+            ref, got, launches = run_both(lib, c, 0)
+            splits, whole = lib.last_split_plan()
+            assert splits > 1 and whole == 0 and launches == 2, (splits, whole, launches)
+            err = np.abs(got - ref)
+            assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
 def test_noalloc_refuses_splits_beyond_its_scratch(lib):
     # 8 splits x 20000 queries x 16 heads x 129 x 4 bytes >> the fixed scratch: refused before any launch.
     st = lib.lib.paged_attn_varlen_noalloc(None, 20000, 16, None, None, 1, 16, 16, 128, lib.PKV_BF16, None, 1, 1,
