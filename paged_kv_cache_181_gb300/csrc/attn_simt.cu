@@ -13,6 +13,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "kv_copy.cuh"
 
 namespace {
@@ -217,12 +219,90 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
   }
 }
 
-// One warp per (token, head): O = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M).
-// Lane s reads split s's log-sum-exp (at most 32 splits), the maximum and the weight sum are
-// warp reductions, and the partial rows are read 8 splits at a time so their loads are in
-// flight together (reading the splits one after another was latency-bound: 28 us for 17 MB).
-// With a split tail (split_direct > 0) only the split items' rows are combined: warp w takes
-// row wi % rows of tensor-core item split_direct + wi / rows, decoded as the kernel decodes it.
+// NC consecutive output values of one lane, rounded to T (one 4-, 8- or 16-byte store).
+template <typename T, int NC>
+PKV_DEVINLINE void store_lane(T* dst, const float* v) {
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (NC == 4)
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+    else
+      *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+  } else {
+    uint32_t p[NC / 2];
+#pragma unroll
+    for (int e = 0; e < NC / 2; ++e) {
+      const T lo = pkv_from_f32<T>(v[2 * e]), hi = pkv_from_f32<T>(v[2 * e + 1]);
+      p[e] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
+             ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+    }
+    if constexpr (NC == 4)
+      *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = p[0];
+  }
+}
+
+// One (token, head) row by one warp: O = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M).  Lane l
+// holds columns [l NC, l NC + NC) (NC = D / 32) and reads them as one vector per split; lane s reads
+// split s's log-sum-exp (at most 32 splits).  The first eight splits' rows are loaded together with
+// the log-sum-exps, so a row with up to eight splits costs one round trip to memory.
+template <typename T, int NC>
+PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
+  using V = typename std::conditional<NC == 4, float4, float2>::type;
+  const int S = a.num_splits;
+  const int64_t stride = a.Tq * a.Hq;  // rows between splits
+  const float* base = a.part_o + item * (32 * NC) + lane * NC;
+  float x[8][NC];
+  auto load = [&](int s0) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      V v;
+      if (s0 + u < S)
+        v = __ldg(reinterpret_cast<const V*>(base + (int64_t)(s0 + u) * stride * (32 * NC)));
+      else
+        memset(&v, 0, sizeof(v));
+      const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) x[u][c] = f[c];
+    }
+  };
+  const float lse = lane < S ? __ldg(a.part_lse + (int64_t)lane * stride + item) : -INFINITY;
+  load(0);
+  float M = lse;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  T* out = (T*)a.out + item * (32 * NC) + lane * NC;
+  float acc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+  if (M == -INFINITY) {  // no split saw a key: 0
+    store_lane<T, NC>(out, acc);
+    return;
+  }
+  const float w = lane < S ? expf(lse - M) : 0.f;  // 0 for an empty split (lse = -inf)
+  float wsum = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  for (int s0 = 0;;) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float ws = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[c] = fmaf(s0 + u < S ? ws : 0.f, x[u][c], acc[c]);
+    }
+    s0 += 8;
+    if (s0 >= S) break;
+    load(s0);
+  }
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] *= inv;
+  store_lane<T, NC>(out, acc);
+}
+
+// One warp per combined (token, head) row.  With a split tail (split_direct > 0) only the split
+// items' rows are combined: warp w takes row wi % rows of tensor-core item split_direct + wi / rows,
+// decoded as the kernel decodes it.
 template <typename T>
 __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
   const int64_t wi = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -246,40 +326,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
   } else if (item >= a.Tq * a.Hq) {
     return;
   }
-  const int S = a.num_splits;
-  const int64_t stride = a.Tq * a.Hq;
-  const float lse = lane < S ? a.part_lse[(int64_t)lane * stride + item] : -INFINITY;
-  float M = lse;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  T* out = (T*)a.out + item * a.D;
-  if (M == -INFINITY) {
-    for (int d = lane; d < a.D; d += 32) out[d] = pkv_from_f32<T>(0.f);
-    return;
-  }
-  const float w = lane < S ? expf(lse - M) : 0.f;  // 0 for an empty split (lse = -inf)
-  float wsum = w;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  const int nc = a.D / 32;  // columns per lane: 2 or 4
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const float* base = a.part_o + item * a.D + lane;
-  for (int s0 = 0; s0 < S; s0 += 8) {
-    float x[8][4];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        x[u][c] = (s0 + u < S && c < nc) ? __ldg(base + ((int64_t)(s0 + u) * stride) * a.D + 32 * c) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float ws = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c] = fmaf(s0 + u < S ? ws : 0.f, x[u][c], acc[c]);
-    }
-  }
-  const float inv = 1.f / wsum;
-  for (int c = 0; c < nc; ++c) out[lane + 32 * c] = pkv_from_f32<T>(acc[c] * inv);
+  if (a.D == 128)
+    combine_row<T, 4>(a, item, lane);
+  else
+    combine_row<T, 2>(a, item, lane);
 }
 
 template <typename T>

@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int dh = 0; dh < D / 64; ++dh)
           ptx::tma_store_3d(&maps.o, dh * 64, h, q0 + i0 + grp * BM, tile + dh * (BM * 128));
         ptx::bulk_commit();
-        ptx::bulk_wait_all();  // done before the CTA (and its shared memory) goes away
+        ptx::bulk_wait_read_all();  // shared memory read before the CTA (and its shared memory) goes away
       }
     } else if (ok) {
       if (!valid) {

@@ -98,8 +98,9 @@ PKV_DEVINLINE void tma_store_3d(const void* tmap, int x, int y, int z, const voi
                : "memory");
 }
 PKV_DEVINLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every bulk store this thread committed has completed.
-PKV_DEVINLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every bulk store this thread committed has read its shared-memory source (the
+// global writes complete on their own; the kernel's completion orders them for later work).
+PKV_DEVINLINE void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 PKV_DEVINLINE void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
