@@ -397,7 +397,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v10"
+KERNEL_REV = "tc-v11"
 
 
 def measure_graph(case, steps: int, fused: bool, main_ms_step: float) -> dict:
@@ -603,6 +603,10 @@ def run_e2e(case, args, world, stream, fused: bool):
     names = ["slots", "block_table", "query_start_loc", "seq_lens", "segs", "seg_start"]
     step_no = [0]
 
+    # Each layer's uploads timed between events on the copy stream (after its wait): their sum in a step
+    # against upload_ms_alone says whether the uploads slow down while the attention runs.
+    up_t = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+
     def e2e_step():
         k = step_no[0] % 2
         step_no[0] += 1
@@ -613,10 +617,12 @@ def run_e2e(case, args, world, stream, fused: bool):
             meta_landed[k].record(up)
             for l in range(layers):
                 up.wait_event(computed[l])  # the previous step no longer reads this layer's inputs
+                up_t[l][0].record(up)
                 case.q[l].copy_(host_q[l], non_blocking=True)
                 case.k_new[l].copy_(host_k[l], non_blocking=True)
                 case.v_new[l].copy_(host_v[l], non_blocking=True)
                 landed[l].record(up)
+                up_t[l][1].record(up)
         for name, t in zip(names, meta_sets[k]):
             setattr(case, name, t)
         stream.wait_event(meta_landed[k])
@@ -670,7 +676,8 @@ def run_e2e(case, args, world, stream, fused: bool):
     api = "paged_kv_write_attn" if fused else "paged_kv_write + paged_attn_varlen"
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
-            "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9}
+            "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
+            "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers))}
 
 
 def main():

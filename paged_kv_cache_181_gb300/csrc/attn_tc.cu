@@ -272,6 +272,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n_q = i0 + BM < Sq ? 2 : 1;  // query tiles with rows in them
 
+  // Softmax groups: warps 4-7 own query tile 0, warps 8-11 tile 1; TMEM lane quarter = warp % 4.
+  // Each row's key limit is read from the segments here, overlapping the set-up below.
+  const int grp = warp >= 8 ? 1 : 0;
+  const bool is_softmax = warp >= 4;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const int i = i0 + grp * BM + row;  // local query index of this thread's row
+  int lim = 0;
+  if (is_softmax && i < Sq) {
+    bool uncovered = false;
+    int s_begin = 0, s_end = 0;
+    if (a.segs) {
+      s_begin = a.seg_start[b];
+      s_end = a.seg_start[b + 1];
+    }
+    const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
+    lim = pkv_row_limit(base + i, L, a.segs, s_begin, s_end, &uncovered);
+    if (a.check && (uncovered || base < 0 || base + Sq > L)) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
+  }
+
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
     for (int s = 0; s < C::NSLOT; ++s) {
@@ -312,25 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // Softmax groups: warps 4-7 own query tile 0, warps 8-11 tile 1; TMEM lane quarter = warp % 4.
-  const int grp = warp >= 8 ? 1 : 0;
-  const bool is_softmax = warp >= 4;
-  const int quarter = warp & 3;
-  const int row = quarter * 32 + lane;
-  const int i = i0 + grp * BM + row;  // local query index of this thread's row
-  int lim = 0;
-  if (is_softmax && i < Sq) {
-    bool uncovered = false;
-    int s_begin = 0, s_end = 0;
-    if (a.segs) {
-      s_begin = a.seg_start[b];
-      s_end = a.seg_start[b + 1];
-    }
-    const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
-    lim = pkv_row_limit(base + i, L, a.segs, s_begin, s_end, &uncovered);
-    if (a.check && (uncovered || base < 0 || base + Sq > L)) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
+  if (is_softmax) {  // the CTA's largest key limit (warp maxima first)
+    const int wmax = __reduce_max_sync(0xffffffffu, lim);
+    if (lane == 0) atomicMax(&sm.lim_max, wmax);
   }
-  if (is_softmax) atomicMax(&sm.lim_max, lim);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -587,14 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // mma_done completes exactly once, after every MMA of the CTA.
         if (__all_sync(0xffffffffu, ptx::mbar_wait(&sm.mma_done, 0, &sm.abort, kWaitLimitNs))) {
           ptx::tc_fence_after();
+          // All of the row's O columns in flight at once, one wait.
+          uint32_t r[D / 32][32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r[c]);
+          ptx::tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence32(r);
+            ptx::reg_fence32(r[c]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(r[e]);
+            for (int e = 0; e < 32; ++e) o[c * 32 + e] = __uint_as_float(r[c][e]);
           }
         } else {
           note_abort(sm, a.err);
