@@ -444,10 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (j > 0 || ks > 0) ? 1u : 0u);
       };
       if (ok) ok = slot_ready(0);
-      if (ok) {
+      if (ok)
         for (int w = 0; w < n_q; ++w) qk(w, 0);
-        ptx::mma_commit(&sm.empty[0]);  // key tile 0 consumed
-      }
       for (int j = 0; ok && j < n; ++j) {
         const bool next = j + 1 < n;
         if (!slot_ready(2 * j + 1)) {  // value tile j
@@ -461,14 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           pv(w, j);
-          if (w == n_q - 1) ptx::mma_commit(&sm.empty[(2 * j + 1) % C::NSLOT]);  // value tile j consumed
           if (next) {
             if (w == 0 && !slot_ready(2 * j + 2)) {  // key tile j+1
               ok = false;
               break;
             }
             qk(w, j + 1);
-            if (w == n_q - 1) ptx::mma_commit(&sm.empty[(2 * j + 2) % C::NSLOT]);  // key tile j+1 consumed
           }
         }
       }
@@ -500,6 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      // Ring slots are released here rather than by MMA commits (each commit in the MMA stream
+      // cost it ~150 cycles): the last group's scores of tile j are committed after every earlier
+      // MMA, so key tile j and value tile j-1 are no longer read.
+      if (grp == n_q - 1 && row == 0) {
+        ptx::mbar_arrive(&sm.empty[(2 * j) % C::NSLOT]);
+        if (j > 0) ptx::mbar_arrive(&sm.empty[(2 * j - 1) % C::NSLOT]);
+      }
       float s[BN];
       {
         uint32_t r[BN / 32][32];
@@ -533,22 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of its rows needs it (alpha = 1 for the others).  P.V of tile j-1 is complete:
       // the score MMA of tile j, whose completion was just observed, was issued after it.
       const bool need = m_tile > m_ref + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ptx::ex2(m_ref - m_tile) : 1.f;  // 0 on a row's first visible tile
+      const bool rescale = __any_sync(0xffffffffu, need);
+      const float alpha = need ? ptx::ex2(m_ref - m_tile) : 1.f;  // 0 on a row's first visible tile
+      if (need) {
         l *= alpha;
-        if (j > 0) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence32(r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            ptx::tmem_st32(tmem + lane_base + O_COL[grp] + c * 32, r);
-          }
-        }
-        if (need) m_ref = m_tile;
+        m_ref = m_tile;
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
@@ -572,6 +564,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st32(tmem + lane_base + S_COL + c * 32, r);
       }
       l += (l0 + l1) + (l2 + l3);
+      // O carries the previous maximum: rescale it before this tile's P.V accumulates into it
+      // (the MMA warp issues that only after the arrive below).  Done once the scores are dead,
+      // so the O chunk does not compete with them for registers.
+      if (rescale && j > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tmem + lane_base + O_COL[grp] + c * 32, r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence32(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          ptx::tmem_st32(tmem + lane_base + O_COL[grp] + c * 32, r);
+        }
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.p_full[grp]);
