@@ -356,7 +356,7 @@ def run_ours(args, world, rank, local):
     split_kv = measure_split_kv(stream, peaks) if not args.no_packed else None
 
     # e2e: inputs from pinned host memory every step, outputs back to the host.
-    e2e = run_e2e(case, args, world, stream, fused) if not args.no_e2e else None
+    e2e = run_e2e(case, args, world, stream, fused, local) if not args.no_e2e else None
 
     result = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -569,7 +569,7 @@ def read_traffic(workload_name: str):
     return int(m.group(3))
 
 
-def run_e2e(case, args, world, stream, fused: bool):
+def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     """The same forward through the public API with every input coming from pinned host memory.
 
     Per step: the per-forward metadata and every layer's Q, new K and new V are copied host -> device on a
@@ -664,12 +664,13 @@ def run_e2e(case, args, world, stream, fused: bool):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    up.wait_event(start)  # no upload of the timed steps starts before the clock does
-    for _ in range(steps):
-        e2e_step()
-    end.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:  # clocks while copies and compute overlap (power draw differs)
+        start.record(stream)
+        up.wait_event(start)  # no upload of the timed steps starts before the clock does
+        for _ in range(steps):
+            e2e_step()
+        end.record(stream)
+        torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
     flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * layers * world
@@ -677,7 +678,8 @@ def run_e2e(case, args, world, stream, fused: bool):
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
             "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
-            "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers))}
+            "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers)),
+            "clocks": clk.summary()}
 
 
 def main():
