@@ -606,6 +606,9 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     # Each layer's uploads timed between events on the copy stream (after its wait): their sum in a step
     # against upload_ms_alone says whether the uploads slow down while the attention runs.
     up_t = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    # Each layer's compute timed the same way (after its waits): their sum against the step says whether the
+    # compute itself slowed down or waited for its inputs.
+    cp_t = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
 
     def e2e_step():
         k = step_no[0] % 2
@@ -629,12 +632,14 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
         for l in range(layers):
             stream.wait_event(landed[l])
             stream.wait_event(fetched[l])  # the previous step's output of this layer has been read back
+            cp_t[l][0].record(stream)
             if fused:
                 case.write_attend(l, stream=stream)
             else:
                 case.write(l, stream=stream)
                 case.attend(l, stream=stream)
             computed[l].record(stream)
+            cp_t[l][1].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(computed[l])
                 host_out[l].copy_(case.out[l], non_blocking=True)
@@ -679,6 +684,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
             "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
             "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
             "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers)),
+            "compute_ms_in_last_step": sum(cp_t[l][0].elapsed_time(cp_t[l][1]) for l in range(layers)),
             "clocks": clk.summary()}
 
 
