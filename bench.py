@@ -31,6 +31,13 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# Host<->device copies overlap kernels only when their stream and the compute stream use different hardware
+# work queues.  With the default 8 queues the end-to-end step was seen to run its uploads after the compute
+# (the step time was exactly the sum of the two) in some processes and not in others; asking for the
+# maximum makes a shared queue unlikely.  Set before CUDA starts; it configures this process's context only.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
+
 METRIC = "paged attention TFLOP/s (% bf16 peak); KV-write GB/s (% HBM peak)"
 DEFAULT_WORKLOAD = "long-window-40L-bf16"
 
@@ -685,6 +692,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
             "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
             "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers)),
             "compute_ms_in_last_step": sum(cp_t[l][0].elapsed_time(cp_t[l][1]) for l in range(layers)),
+            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
             "clocks": clk.summary()}
 
 
