@@ -582,6 +582,9 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     Per step: the per-forward metadata and every layer's Q, new K and new V are copied host -> device on a
     copy stream, each layer's write + attention runs on the compute stream as soon as its inputs have
     landed, and each layer's output is copied device -> host on a third stream as soon as it is ready.
+    Alternate steps use two device copies of the inputs and outputs, so that a step's uploads never wait
+    for the previous step's compute of the same layer (uploads run slower while the attention runs on
+    some machines; with one copy that coupled the two streams layer by layer).
     """
     import torch
 
@@ -599,9 +602,13 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     up = torch.cuda.Stream()
     down = torch.cuda.Stream()
-    landed = [torch.cuda.Event() for _ in range(layers)]
-    computed = [torch.cuda.Event() for _ in range(layers)]
-    fetched = [torch.cuda.Event() for _ in range(layers)]
+    # Two device sets of the per-layer inputs and outputs, used by alternate steps.
+    io_sets = [(case.q, case.k_new, case.v_new, case.out),
+               ([t.clone() for t in case.q], [t.clone() for t in case.k_new], [t.clone() for t in case.v_new],
+                [torch.empty_like(t) for t in case.out])]
+    landed = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
+    computed = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
+    fetched = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
     # Two device copies of the per-forward metadata, used by alternate steps, so that a step's metadata
     # upload does not wait for the previous step's last layer.
     meta_sets = [meta_dev, [t.clone() for t in meta_dev]]
@@ -620,42 +627,45 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     def e2e_step():
         k = step_no[0] % 2
         step_no[0] += 1
+        q_d, k_d, v_d, o_d = io_sets[k]
         with torch.cuda.stream(up):
             up.wait_event(meta_free[k])
             for hd, dd in zip(meta_host, meta_sets[k]):
                 dd.copy_(hd, non_blocking=True)
             meta_landed[k].record(up)
             for l in range(layers):
-                up.wait_event(computed[l])  # the previous step no longer reads this layer's inputs
+                up.wait_event(computed[k][l])  # the step before last no longer reads this set's inputs
                 up_t[l][0].record(up)
-                case.q[l].copy_(host_q[l], non_blocking=True)
-                case.k_new[l].copy_(host_k[l], non_blocking=True)
-                case.v_new[l].copy_(host_v[l], non_blocking=True)
-                landed[l].record(up)
+                q_d[l].copy_(host_q[l], non_blocking=True)
+                k_d[l].copy_(host_k[l], non_blocking=True)
+                v_d[l].copy_(host_v[l], non_blocking=True)
+                landed[k][l].record(up)
                 up_t[l][1].record(up)
         for name, t in zip(names, meta_sets[k]):
             setattr(case, name, t)
+        case.q, case.k_new, case.v_new, case.out = q_d, k_d, v_d, o_d
         stream.wait_event(meta_landed[k])
         for l in range(layers):
-            stream.wait_event(landed[l])
-            stream.wait_event(fetched[l])  # the previous step's output of this layer has been read back
+            stream.wait_event(landed[k][l])
+            stream.wait_event(fetched[k][l])  # this set's output of the step before last has been read back
             cp_t[l][0].record(stream)
             if fused:
                 case.write_attend(l, stream=stream)
             else:
                 case.write(l, stream=stream)
                 case.attend(l, stream=stream)
-            computed[l].record(stream)
+            computed[k][l].record(stream)
             cp_t[l][1].record(stream)
             with torch.cuda.stream(down):
-                down.wait_event(computed[l])
-                host_out[l].copy_(case.out[l], non_blocking=True)
-                fetched[l].record(down)
+                down.wait_event(computed[k][l])
+                host_out[l].copy_(o_d[l], non_blocking=True)
+                fetched[k][l].record(down)
         meta_free[k].record(stream)
         stream.wait_stream(down)
 
-    for ev in fetched + computed + meta_free:
+    for ev in fetched[0] + fetched[1] + computed[0] + computed[1] + meta_free:
         ev.record(stream)
+    e2e_step()
     e2e_step()
     torch.cuda.synchronize()
     # One step's uploads alone, without compute: the host->device bandwidth this machine gives, so that an
@@ -666,9 +676,9 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
         for hd, dd in zip(meta_host, meta_sets[0]):
             dd.copy_(hd, non_blocking=True)
         for l in range(layers):
-            case.q[l].copy_(host_q[l], non_blocking=True)
-            case.k_new[l].copy_(host_k[l], non_blocking=True)
-            case.v_new[l].copy_(host_v[l], non_blocking=True)
+            io_sets[0][0][l].copy_(host_q[l], non_blocking=True)
+            io_sets[0][1][l].copy_(host_k[l], non_blocking=True)
+            io_sets[0][2][l].copy_(host_v[l], non_blocking=True)
         u1.record(up)
     torch.cuda.synchronize()
     upload_ms = u0.elapsed_time(u1)
@@ -684,6 +694,10 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
+    # The case's tensors again those it started with (the second set and its events go with this function).
+    case.q, case.k_new, case.v_new, case.out = io_sets[0]
+    for name, t in zip(names, meta_sets[0]):
+        setattr(case, name, t)
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
     flops = 4 * case.w.head_dim * case.w.num_heads * visible_pairs(case.meta) * layers * world
     api = "paged_kv_write_attn" if fused else "paged_kv_write + paged_attn_varlen"
