@@ -601,6 +601,9 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v + meta_host)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     up = torch.cuda.Stream()
+    # K and V of a layer upload on streams of their own beside Q's, so that copies can use more than one copy
+    # engine at a time.
+    up_k, up_v = torch.cuda.Stream(), torch.cuda.Stream()
     down = torch.cuda.Stream()
     # Two device sets of the per-layer inputs and outputs, used by alternate steps.
     io_sets = [(case.q, case.k_new, case.v_new, case.out),
@@ -636,9 +639,15 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
             for l in range(layers):
                 up.wait_event(computed[k][l])  # the step before last no longer reads this set's inputs
                 up_t[l][0].record(up)
+                up_k.wait_stream(up)
+                up_v.wait_stream(up)
                 q_d[l].copy_(host_q[l], non_blocking=True)
-                k_d[l].copy_(host_k[l], non_blocking=True)
-                v_d[l].copy_(host_v[l], non_blocking=True)
+                with torch.cuda.stream(up_k):
+                    k_d[l].copy_(host_k[l], non_blocking=True)
+                with torch.cuda.stream(up_v):
+                    v_d[l].copy_(host_v[l], non_blocking=True)
+                up.wait_stream(up_k)
+                up.wait_stream(up_v)
                 landed[k][l].record(up)
                 up_t[l][1].record(up)
         for name, t in zip(names, meta_sets[k]):
