@@ -174,14 +174,6 @@ PKV_DEVINLINE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
-PKV_DEVINLINE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16};" ::"r"(taddr),
-      PKV_W8(0), PKV_W8(8)
-      : "memory");
-}
-
 // Ties 32 registers to a point in the program: uses after this statement cannot be
 // hoisted above it (used right after tcgen05.wait::ld).
 PKV_DEVINLINE void reg_fence32(uint32_t (&r)[32]) {
