@@ -35,7 +35,11 @@
 //              on its scores the tensor core runs the other group's MMAs.  An
 //              MMA issue returns when the pipe takes it, so the issue code is
 //              kept lean (descriptors built once, offset per MMA);
-//   warps 2-3  fused write + attention only: the slot-mapping scatter of the
+//   warp 3     producer of the value tiles (warp 0 then loads Q and the key
+//              tiles only): each producer warp shares an SM partition with two
+//              softmax warps, and halving the per-tile instructions on one
+//              partition shortened the softmax pass that is the critical path;
+//   warp 2     fused write + attention only: the slot-mapping scatter of the
 //              new k/v (this CTA's share of the rows);
 //   warps 4-7  softmax of query tile 0, warps 8-11 of tile 1: one query row per
 //              thread (TMEM lane = row).  Reads a score row from TMEM, masks,
@@ -206,12 +210,11 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const OperandMaps& m, uint64_t* full,
 
 // Fused call: this CTA's share of the slot-mapping scatter, by warps 2 and 3 (idle otherwise).
 PKV_DEVINLINE void fused_write_share(const PkvAttnArgs& a, int warp, int lane) {
-  if (a.k_new == nullptr || (warp != 2 && warp != 3)) return;
+  if (a.k_new == nullptr || warp != 2) return;
   const int64_t cta = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
   const int vec_per_row = a.Hkv * a.D * 2 / 16;
   pkv_scatter((const uint4*)a.k_new, (const uint4*)a.v_new, a.slots, a.Tq, (uint4*)a.k_pool, (uint4*)a.v_pool,
-              a.num_slots, vec_per_row, a.err, a.check, cta * 2 + (warp - 2), (int64_t)gridDim.x * gridDim.y * 2, lane,
-              &a);
+              a.num_slots, vec_per_row, a.err, a.check, cta, (int64_t)gridDim.x * gridDim.y, lane, &a);
 }
 
 template <int D, bool BF16>
@@ -354,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
   ptx::regs_dec<kRegsLow>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ producers: warp 0 key tiles, warp 3 value tiles
     // Keys at the queries' own positions [cb, ce) (fused call: read from the new tokens).
     int cb = 0, ce = 0;
     if (a.k_new) {
@@ -371,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const OperandMaps km{&maps.kb, &maps.kc, &maps.k1, &maps.kn5, &maps.kn8, &maps.kn1};
     const OperandMaps vm{&maps.vb, &maps.vc, &maps.v1, &maps.vn5, &maps.vn8, &maps.vn1};
-    if (n == 0 && lane == 0) {
+    if (warp == 0 && n == 0 && lane == 0) {
       // No key tile to process: nothing will wait for Q, but its copy must land before the CTA exits.
       int never = 0;
       ptx::mbar_wait(&sm.q_full, 0, &never, kWaitLimitNs);
     }
-    for (int idx = 0; idx < 2 * n; ++idx) {
+    for (int idx = warp == 0 ? 0 : 1; idx < 2 * n; idx += 2) {
       if (__any_sync(0xffffffffu, sm.abort != 0)) break;
       const int pos = idx % C::NSLOT, use = idx / C::NSLOT;
       const bool is_v = idx & 1;
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       load_tile<D>(sm.kv[pos], is_v ? vm : km, &sm.full[pos], a, b, kvh, kt, rows, cb, ce, q0, lane);
     }
-    if (sm.abort && lane == 0) {
+    if (warp == 0 && sm.abort && lane == 0) {
       // Let copies already issued land before the shared memory goes away.
       int dummy = 0;
       ptx::mbar_wait(&sm.q_full, 0, &dummy, kWaitLimitNs);
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_wait(&sm.mma_done, 0, &dummy, kWaitLimitNs);
     }
   } else {
-    // ------------------------------------------------------------ warps 2-3: fused write
+    // ------------------------------------------------------------ warp 2: fused write
     fused_write_share(a, warp, lane);
   }
   } else {
