@@ -208,7 +208,7 @@ PKV_DEVINLINE void load_tile(uint8_t* dst, const OperandMaps& m, uint64_t* full,
   }
 }
 
-// Fused call: this CTA's share of the slot-mapping scatter, by warps 2 and 3 (idle otherwise).
+// Fused call: this CTA's share of the slot-mapping scatter, by warp 2 (idle otherwise).
 PKV_DEVINLINE void fused_write_share(const PkvAttnArgs& a, int warp, int lane) {
   if (a.k_new == nullptr || warp != 2) return;
   const int64_t cta = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
