@@ -214,6 +214,8 @@ PKV_API pkv_status paged_kv_write(const void* k, const void* v, const int64_t* s
  *   slot_mapping  device int64 [Tq]
  *   everything else as paged_attn_varlen; key_pool/value_pool are written (num_blocks*16 slots).
  * Tokens of different rows must not share pool blocks.  Splits add the combine launch.
+ * Empty sizes (Tq, B or max_query_len == 0) return PKV_OK without a launch: no token is
+ * written either.
  */
 PKV_API pkv_status paged_kv_write_attn(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
                                        int64_t Tq, int Hq, void* key_pool, void* value_pool, int64_t num_blocks,
@@ -283,6 +285,8 @@ PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int m
  *   max_query_len    >= every row's Sq;  max_seq_len >= every L, <= W * 16
  *   softmax_scale    multiplies Q.K (the pages pass D^-0.5)
  * A query that sees no key (only possible with ill-formed segments) gets 0.
+ * Tq == 0, B == 0 or max_query_len == 0: nothing to compute; PKV_OK without a launch
+ * (sizes and the dtype are still validated; out is not touched).
  * The softmax statistics and both products accumulate in fp32.
  * Supported: dt in {F32, BF16, F16}; D in {64, 128}; block_size 16; Hq % Hkv == 0.
  */

@@ -170,3 +170,16 @@ def test_table_errors(lib):
         lib.table_width(0, 1, 1, 0)
     with pytest.raises(lib.PkvError):
         lib.visible_window([1], 40, 0, 40)  # too few row blocks
+
+
+def test_empty_attention_calls_are_no_ops(lib):
+    # Empty sizes return before any pointer is read or any CUDA call is made (also without a GPU).
+    for tq, b, max_q in ((0, 1, 1), (4, 0, 1), (4, 1, 0)):
+        st = lib.lib.paged_attn_varlen(None, tq, 4, None, None, 1, 16, 2, 64, 1, None, b, 1, None, None, max_q, 16,
+                                       1.0, None, None, None, None, 0, 0, None)
+        assert st == lib.PKV_OK, (tq, b, max_q, lib.last_error())
+        assert lib.last_launches() == 0
+        st = lib.lib.paged_kv_write_attn(None, None, None, None, tq, 4, None, None, 1, 16, 2, 64, 1, None, b, 1,
+                                         None, None, max_q, 16, 1.0, None, None, None, None, 0, 0, None)
+        assert st == lib.PKV_OK, (tq, b, max_q, lib.last_error())
+        assert lib.last_launches() == 0
