@@ -75,10 +75,11 @@ def oracle_pools(w: Workload, d: synth.Draw, oc: OracleCase) -> None:
     oc.k_pool, oc.v_pool, oc.q = kp, vp, to_np(d.q)
 
 
-def expected(w: Workload, oc: OracleCase, sample=None, scale=None) -> np.ndarray:
+def expected(w: Workload, oc: OracleCase, sample=None, scale=None, dtype=np.float64) -> np.ndarray:
+    """Oracle outputs in float64 (or the float32 twin, within 1e-5 of it, for whole layers)."""
     scale = w.head_dim ** -0.5 if scale is None else scale
     return pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, scale,
-                              w.block_size, oc.segments, sample=sample)
+                              w.block_size, oc.segments, sample=sample, dtype=dtype)
 
 
 def sample_rows(w: Workload, per_head: int, seed: int = 0) -> dict:

@@ -1,4 +1,5 @@
-"""GPU: bounds-check mode, empty rows, ragged batches, and the long-window workload at full size.
+"""GPU: bounds-check mode, empty rows, ragged batches, and the long-window workload at full size
+(40 layers on sampled rows; one layer on every output).
 
 Bad metadata is only ever handed to kernels with PKV_CHECK_BOUNDS set: they
 skip the offending access and raise the device error word (no fault, no trap).
@@ -120,6 +121,29 @@ def test_long_window_forty_layers_full_size(lib, fused):
         want = cases.expected(w, oc, sample)
         max_abs, mean_abs = cases.compare(case.out[layer].float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
         assert max_abs <= 2e-2 and mean_abs <= 2e-3, (layer, max_abs, mean_abs)
+
+
+def test_long_window_layer_zero_every_output(lib):
+    """Every output of one layer of the benchmarked workload, through the call bench.py times
+    (the fused write + attention with its split tail): 2 rows x 40 heads x 1560 queries over
+    26520 keys, against the float32 oracle twin (within 1e-5 of float64, pinned on the CPU)."""
+    from paged_kv_cache_181_gb300 import synth, workload
+
+    w = configs.LONG_WINDOW
+    case = workload.build_case(w, device="cuda", poison=False, layers=1, data_device="cpu")
+    case.step(fused=True)
+    torch.cuda.synchronize()
+    assert lib.check() == 0
+    splits, whole = lib.last_split_plan()
+    assert splits > 1 and whole > 0  # the split tail behind whole waves, as in the bench
+    d = synth.draw(w, 0, device="cpu")  # the same seeded draw the case made
+    assert torch.equal(d.q, case.q[0].cpu())
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, d, oc)
+    want = cases.expected(w, oc, dtype=np.float32).astype(np.float64)
+    assert not np.isnan(want).any()
+    max_abs, mean_abs = cases.compare(case.out[0].float().cpu().numpy(), want, w.dtype)
+    assert max_abs <= 2e-2 and mean_abs <= 2e-3, (max_abs, mean_abs)
 
 
 def test_expired_wait_reports_timeout_and_leaves_the_context_usable(lib):
