@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, layout or metadata seen on the host */
-  PKV_ERR_UNSUPPORTED = 2,  /* dtype, head dim or block size this build does not handle */
+  PKV_ERR_UNSUPPORTED = 2,  /* dtype, head dim or block size the library does not handle */
   PKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   PKV_ERR_DEVICE_CHECK = 4, /* a kernel in PKV_CHECK_BOUNDS mode saw bad metadata */
   PKV_ERR_CAPACITY = 5      /* an output buffer or workspace is too small */
