@@ -130,3 +130,21 @@ def test_validate_spans_rejects(spans, offset, qlen, seq_len):
 
 def test_validate_spans_accepts_touching_spans():
     pa.validate_spans([(0, 2), (2, 5)], 1, 4, 5)
+
+
+@pytest.mark.parametrize("seq_len", [6, 8, 10])
+def test_segments_match_direct_mask_exhaustive_three_spans(seq_len):
+    # Every set of exactly three ordered, non-overlapping spans (touching allowed), at every query
+    # offset and length: the case the random test above only samples.
+    n = 0
+    for spans in all_span_sets(seq_len, 3):
+        if len(spans) != 3:
+            continue
+        for offset in range(seq_len):
+            for qlen in range(1, seq_len - offset + 1):
+                segs = pa.build_segments(list(spans), offset, qlen)
+                got = mask_from_segments(segs, offset, qlen, seq_len)
+                want = direct_mask(spans, offset, qlen, seq_len)
+                assert (got == want).all(), (spans, offset, qlen, segs)
+                n += 1
+    assert n > 0
