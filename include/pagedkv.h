@@ -342,8 +342,10 @@ PKV_API pkv_status paged_attn_varlen_noalloc(const void* q, int64_t Tq, int Hq, 
 PKV_API pkv_status pkv_check(void* stream, uint32_t* bits);
 
 /*
- * pkv_last_launches -- number of kernels the last paged_kv_write /
- * paged_attn_varlen call on this thread launched (0 if it launched nothing).
+ * pkv_last_launches -- number of kernels the last device call on this thread
+ * (paged_kv_write, paged_kv_gather, paged_attn_varlen, paged_kv_write_attn,
+ * paged_attn_varlen_noalloc, pkv_selftest_wait) launched: 0 when it launched nothing, 2 for an
+ * attention call that split (the attention and its combine).
  */
 PKV_API int pkv_last_launches(void);
 
@@ -357,8 +359,8 @@ PKV_API int pkv_last_launches(void);
 PKV_API void pkv_last_split_plan(int* splits, int64_t* whole_items);
 
 /*
- * pkv_sm_count -- number of SMs of the current device (used to size
- * persistent grids and key-range splits); -1 on error.
+ * pkv_sm_count -- number of SMs of the current device (what the key-range
+ * split planning counts waves in); -1 on error.
  */
 PKV_API int pkv_sm_count(void);
 
