@@ -191,12 +191,40 @@ def _dptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _require(fn: str, *tensors) -> None:
+    """Every tensor (None skipped) contiguous and on the current CUDA device.
+
+    The library takes raw device pointers: a host tensor's address would reach the kernels, and a
+    tensor of another device would be launched on this device's stream.
+    """
+    torch = _torch()
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{fn}: tensors must be on a CUDA device (got {t.device})")
+        if not t.is_contiguous():
+            raise ValueError(f"{fn}: tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+            if dev.index is not None and dev.index != torch.cuda.current_device():
+                raise ValueError(f"{fn}: tensors are on {dev}, the current device is cuda:{torch.cuda.current_device()}")
+        elif t.device != dev:
+            raise ValueError(f"{fn}: tensors must be on one device")
+
+
+def _require_metadata(fn: str, *tensors) -> None:
+    torch = _torch()
+    for t in tensors:
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{fn}: metadata must be int32")
+
+
 def paged_kv_write(k, v, slot_mapping, key_pool, value_pool, *, flags: int = 0, stream=None) -> None:
     """key_pool[slot[t]] = k[t]; value_pool[slot[t]] = v[t] (pools ``[num_slots, Hkv, D]``)."""
     T, hkv, d = k.shape
-    for t in (k, v, key_pool, value_pool):
-        if not t.is_contiguous():
-            raise ValueError("paged_kv_write: tensors must be contiguous")
+    _require("paged_kv_write", k, v, slot_mapping, key_pool, value_pool)
     if v.shape != k.shape or key_pool.shape != value_pool.shape or key_pool.shape[1:] != k.shape[1:]:
         raise ValueError("paged_kv_write: shape mismatch")
     if k.dtype != key_pool.dtype or v.dtype != value_pool.dtype or k.dtype != v.dtype:
@@ -214,9 +242,7 @@ def paged_kv_gather(key_pool, value_pool, block_table, stage_k, stage_v, *, firs
     B, W = block_table.shape
     if n_blocks is None:
         n_blocks = W - first_block
-    for t in (key_pool, value_pool, block_table, stage_k, stage_v):
-        if not t.is_contiguous():
-            raise ValueError("paged_kv_gather: tensors must be contiguous")
+    _require("paged_kv_gather", key_pool, value_pool, block_table, stage_k, stage_v)
     if block_table.dtype != torch.int32:
         raise ValueError("paged_kv_gather: block_table must be int32")
     if stage_k.shape != stage_v.shape or stage_k.shape[0] != B or stage_k.shape[2:] != key_pool.shape[1:]:
@@ -242,14 +268,11 @@ def paged_attn_varlen(q, key_pool, value_pool, block_table, query_start_loc, seq
     hkv = key_pool.shape[1]
     if out is None:
         out = torch.empty_like(q)
-    for t in (q, key_pool, value_pool, block_table, query_start_loc, seq_lens, out):
-        if not t.is_contiguous():
-            raise ValueError("paged_attn_varlen: tensors must be contiguous")
+    _require("paged_attn_varlen", q, key_pool, value_pool, block_table, query_start_loc, seq_lens, segs, seg_start,
+             out, workspace)
     if key_pool.dtype != q.dtype or value_pool.dtype != q.dtype or out.dtype != q.dtype:
         raise ValueError("paged_attn_varlen: q, pools and out must share one dtype")
-    for t in (block_table, query_start_loc, seq_lens) + ((seg_start,) if seg_start is not None else ()):
-        if t.dtype != torch.int32:
-            raise ValueError("paged_attn_varlen: metadata must be int32")
+    _require_metadata("paged_attn_varlen", block_table, query_start_loc, seq_lens, segs, seg_start)
     B, W = block_table.shape
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ok(lib.paged_attn_varlen(_dptr(q), Tq, hq, _dptr(key_pool), _dptr(value_pool), key_pool.shape[0] // block_size,
@@ -269,9 +292,9 @@ def paged_kv_write_attn(q, k, v, slot_mapping, key_pool, value_pool, block_table
     hkv = key_pool.shape[1]
     if out is None:
         out = torch.empty_like(q)
-    for t in (q, k, v, slot_mapping, key_pool, value_pool, block_table, query_start_loc, seq_lens, out):
-        if not t.is_contiguous():
-            raise ValueError("paged_kv_write_attn: tensors must be contiguous")
+    _require("paged_kv_write_attn", q, k, v, slot_mapping, key_pool, value_pool, block_table, query_start_loc, seq_lens,
+             segs, seg_start, out, workspace)
+    _require_metadata("paged_kv_write_attn", block_table, query_start_loc, seq_lens, segs, seg_start)
     if len({q.dtype, k.dtype, v.dtype, key_pool.dtype, value_pool.dtype, out.dtype}) != 1:
         raise ValueError("paged_kv_write_attn: q, k, v, pools and out must share one dtype")
     if k.shape != (Tq, hkv, d) or v.shape != k.shape:
@@ -300,6 +323,11 @@ def paged_attn_varlen_noalloc(q, key_pool, value_pool, block_table, query_start_
     hkv = key_pool.shape[1]
     if out is None:
         out = torch.empty_like(q)
+    _require("paged_attn_varlen_noalloc", q, key_pool, value_pool, block_table, query_start_loc, seq_lens, segs,
+             seg_start, out)
+    if key_pool.dtype != q.dtype or value_pool.dtype != q.dtype or out.dtype != q.dtype:
+        raise ValueError("paged_attn_varlen_noalloc: q, pools and out must share one dtype")
+    _require_metadata("paged_attn_varlen_noalloc", block_table, query_start_loc, seq_lens, segs, seg_start)
     B, W = block_table.shape
     _ok(lib.paged_attn_varlen_noalloc(_dptr(q), Tq, hq, _dptr(key_pool), _dptr(value_pool),
                                       key_pool.shape[0] // block_size, block_size, hkv, d, dtype_code(q),
@@ -310,7 +338,9 @@ def paged_attn_varlen_noalloc(q, key_pool, value_pool, block_table, query_start_
 
 
 def check(stream=None) -> int:
-    """Synchronise, read and clear the device error word; returns its bits (raises PkvError if set)."""
+    """Synchronise, read and clear the device error word; returns its bits (0: clean).
+
+    Raises PkvError only when the call itself fails (no device, a CUDA error on the stream)."""
     bits = C.c_uint32(0)
     st = lib.pkv_check(_stream(stream), C.byref(bits))
     if st not in (PKV_OK, PKV_ERR_DEVICE_CHECK):

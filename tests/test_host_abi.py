@@ -183,3 +183,27 @@ def test_empty_attention_calls_are_no_ops(lib):
                                          None, None, max_q, 16, 1.0, None, None, None, None, 0, 0, None)
         assert st == lib.PKV_OK, (tq, b, max_q, lib.last_error())
         assert lib.last_launches() == 0
+
+
+def test_wrappers_refuse_host_tensors(lib):
+    # The library takes raw device pointers: the binding must stop a host tensor before the C call.
+    import torch
+
+    k = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    slots = torch.arange(4, dtype=torch.int64)
+    pool = torch.zeros(64, 2, 64, dtype=torch.bfloat16)
+    q = torch.zeros(4, 4, 64, dtype=torch.bfloat16)
+    qsl = torch.tensor([0, 4], dtype=torch.int32)
+    seq = torch.tensor([4], dtype=torch.int32)
+    table = torch.zeros(1, 4, dtype=torch.int32)
+    calls = [
+        lambda: lib.paged_kv_write(k, k, slots, pool, pool),
+        lambda: lib.paged_kv_gather(pool, pool, table, torch.zeros(1, 64, 2, 64, dtype=torch.bfloat16),
+                                    torch.zeros(1, 64, 2, 64, dtype=torch.bfloat16)),
+        lambda: lib.paged_attn_varlen(q, pool, pool, table, qsl, seq, 4, 64, 0.125),
+        lambda: lib.paged_attn_varlen_noalloc(q, pool, pool, table, qsl, seq, 4, 64, 0.125),
+        lambda: lib.paged_kv_write_attn(q, k, k, slots, pool, pool, table, qsl, seq, 4, 64, 0.125),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA device"):
+            call()
