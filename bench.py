@@ -177,8 +177,21 @@ def max_over_ranks(x: float, world: int) -> float:
 _ORACLE_CASES: dict = {}
 
 
-def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int | None = None) -> dict:
-    """Time the float32 oracle on a bounded sample of the workload (layer 0, row 0, whole heads)."""
+def _oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        info = threadpool_info()
+        return max(int(i.get("num_threads", 1)) for i in info) if info else (os.cpu_count() or 1)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int | None = None, rows: int = 1) -> dict:
+    """Time the float32 oracle on the workload's layer 0: the first ``rows`` rows (CFG branches), whole
+    (row, head) pairs in order until ``budget_s`` of CPU time has passed (all of them when it is None)."""
+    import dataclasses
+
     import numpy as np
 
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -186,37 +199,75 @@ def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int | None = None) -
     from paged_kv_cache_181_gb300 import synth
     from tests import cases
 
-    import dataclasses
-
-    w1 = dataclasses.replace(w, batch=1, layers=1)
-    oc = _ORACLE_CASES.get(w1.name)
+    w1 = dataclasses.replace(w, batch=rows, layers=1)
+    oc = _ORACLE_CASES.get(w1.name, {}).get(rows)
     if oc is None:  # inputs and pools are built once, outside the timed region
         d = synth.draw(w1, 0, "cpu")
         oc = cases.oracle_metadata(w1)
         cases.oracle_pools(w1, d, oc)
-        _ORACLE_CASES[w1.name] = oc
-    heads = list(range(w1.num_heads if max_heads is None else min(max_heads, w1.num_heads)))
+        _ORACLE_CASES.setdefault(w1.name, {})[rows] = oc
+    n_heads = w1.num_heads if max_heads is None else min(max_heads, w1.num_heads)
+    units = [(b, h) for b in range(rows) for h in range(n_heads)]
+    flops_per_unit = [pa.attention_flops(oc.qsl[b:b + 2] - oc.qsl[b], oc.seq_lens[b:b + 1],
+                                         None if oc.segments is None else oc.segments[b:b + 1], 1, w1.head_dim)
+                      for b in range(rows)]
     flops = 0
     done = 0
     t0 = time.perf_counter()
-    for h in heads:
-        sample = {(0, h): np.arange(w1.q_len)}
+    for b, h in units:
+        sample = {(b, h): np.arange(w1.q_len)}
         pa.paged_attention(oc.q, oc.k_pool, oc.v_pool, oc.table, oc.qsl, oc.seq_lens, w1.head_dim ** -0.5,
                            w1.block_size, oc.segments, dtype=np.float32, sample=sample)
-        flops += pa.attention_flops(oc.qsl, oc.seq_lens, oc.segments, 1, w1.head_dim)
+        flops += flops_per_unit[b]
         done += 1
-        if time.perf_counter() - t0 >= budget_s:
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    try:
-        from threadpoolctl import threadpool_info
+    what = (f"all {rows} rows x {w1.num_heads} heads" if done == len(units) and n_heads == w1.num_heads
+            else f"{done} of {rows * w1.num_heads} (row, head) pairs")
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"{w.name}: layer 0, {what}, {w1.q_len} queries x {int(oc.seq_lens[0])} keys each, "
+                      f"float32 NumPy oracle ({dt:.1f} s)", "seconds": dt}
 
-        cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) if threadpool_info() else os.cpu_count()
-    except Exception:
-        cores = os.cpu_count()
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{w.name}: layer 0, branch 0, {done} of {w.num_heads} heads x {w.q_len} queries x "
-                      f"{int(oc.seq_lens[0])} keys, float32 NumPy oracle ({dt:.1f} s)", "seconds": dt}
+
+def cpu_write_sample(w) -> dict:
+    """Time the oracle's KV write (oracle.pagedattn.kv_write, a row-by-row copy) of one layer's current chunk,
+    K and V, on the workload's own bytes: 16-bit values are handled as uint16 bit patterns, so the bytes
+    moved are those of the GPU write.  The pools are touched once before the timed write."""
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import pagedattn as pa
+    from paged_kv_cache_181_gb300 import synth
+    from tests import cases
+
+    oc = cases.oracle_metadata(w)
+    d = synth.draw(w, 0, "cpu")
+    def host_bits(t):
+        t = t.contiguous()
+        return t.numpy() if w.dtype == "f32" else t.view(torch.int16).numpy().view(np.uint16)
+
+    k, v = host_bits(d.k_cur), host_bits(d.v_cur)
+    bits = k.dtype
+    n_slots = w.pool_blocks * w.block_size
+    kp = np.zeros((n_slots, w.num_kv_heads, w.head_dim), dtype=bits)
+    vp = np.zeros_like(kp)
+    pa.kv_write(kp, oc.slots, k)
+    pa.kv_write(vp, oc.slots, v)
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        pa.kv_write(kp, oc.slots, k)
+        pa.kv_write(vp, oc.slots, v)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    tq = len(oc.slots)
+    nbytes = tq * 2 * (2 * k[0].nbytes) + tq * 8
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{w.name}: one layer's write, {tq} tokens x K and V rows of {k[0].nbytes} B into "
+                      f"{n_slots}-slot pools, oracle kv_write (one Python-level row copy per row, one thread; "
+                      f"median of 3: {dt * 1e3:.1f} ms)", "seconds": dt}
 
 
 def workload_config(w, world: int) -> dict:
@@ -291,17 +342,9 @@ def run_ours(args, world, rank, local):
     ev_w = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
     ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
     write_ms, attn_ms, launch_log = [], [], []
-    # KV write: bursts of one write per layer between two events (a single ~25 us launch is too
-    # short to time alone), each write into its own cold layer pool.
-    wb0, wb1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    write_burst_ms = []
-    for _ in range(3):
-        wb0.record(stream)
-        for l in range(layers):
-            case.write(l, stream=stream)
-        wb1.record(stream)
-        torch.cuda.synchronize()
-        write_burst_ms.append(wb0.elapsed_time(wb1) / layers)
+    # KV write: a burst of one write per layer (a single ~20 us launch is too short to time alone), each
+    # write into its own cold layer pool, replayed from a CUDA graph.
+    write_avg = graph_burst_ms([lambda l=l: case.write(l) for l in range(layers)], stream)
     # The attention launch as the step runs it: the fused write + attention, or (two-call form)
     # the attention call after its layer's write.
     for _ in range(max(1, min(args.steps, 3))):
@@ -340,8 +383,8 @@ def run_ours(args, world, rank, local):
     total_flops = flops_per_layer * layers * world
     value = total_flops / (ms_step * 1e-3) / 1e12
 
+    split_plan = dict(zip(("splits", "whole_items"), _lib.last_split_plan()))
     attn_avg = statistics.mean(attn_ms)
-    write_avg = statistics.median(write_burst_ms)
     attn_tflops = flops_per_layer / (attn_avg * 1e-3) / 1e12
     write_gbs = write_bytes_per_layer / (write_avg * 1e-3) / 1e9
     # Per layer: the attention launch (+ combine when split), plus the write launch in the two-call form.
@@ -398,8 +441,33 @@ def run_ours(args, world, rank, local):
         result["packed_rows"] = packed_rows
     if split_kv is not None:
         result["split_kv"] = split_kv
+    # Every workload at full size, one layer each (the long-window entry is this step's own figures).
+    if not args.no_workloads:
+        wl = {w.name: {
+            "attention": {"api": result["step_api"], "ms_per_call": attn_avg,
+                          "algorithmic_flops_per_call": flops_per_layer, "tflops": attn_tflops,
+                          "frac_of_burst": attn_tflops / peaks["bf16_tflops"],
+                          "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                          "launches_per_call": attn_launches[0], "split_plan": split_plan,
+                          "l2": "each layer reads its own pools (cold)", "dtype": w.dtype},
+            "kv_write": {"us_per_launch": write_avg * 1e3, "algorithmic_bytes_per_launch": write_bytes_per_layer,
+                         "gbs": write_gbs, "frac_of_hbm": write_gbs / peaks["hbm_gbs"],
+                         "burst_launches": layers, "timing": "burst replayed from one CUDA graph",
+                         "row_bytes": row_bytes, "rows": 2 * tq},
+            "clocks": result["clocks"]}}
+        for name in OTHER_WORKLOADS:
+            if name != w.name:
+                wl[name] = measure_workload(name, stream, peaks)
+        result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = {k: v for k, v in cpu_oracle_sample(w).items() if k != "seconds"}
+        from paged_kv_cache_181_gb300 import configs as _cfg
+
+        main_cpu = cpu_oracle_sample(w)
+        extra = [cpu_oracle_sample(_cfg.ONE_FRAME, budget_s=None, rows=2),
+                 cpu_oracle_sample(_cfg.MIXED_MASK, budget_s=None, rows=2),
+                 cpu_write_sample(_cfg.LONG_WINDOW), cpu_write_sample(_cfg.MIXED_MASK)]
+        result["cpu_baseline"] = {k: v for k, v in main_cpu.items() if k != "seconds"} | {
+            "cases": [{k: v for k, v in c.items() if k != "seconds"} for c in extra]}
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -559,6 +627,119 @@ def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
         "chunk_rows": chunk_rows,
     }
     del st
+    torch.cuda.empty_cache()
+    return res
+
+
+OTHER_WORKLOADS = ("tiny-f32", "one-frame-bf16", "gqa-action-bf16", "mixed-mask-bf16")
+
+
+def _l2_bytes() -> int:
+    import torch
+
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 2**20
+
+
+def graph_burst_ms(calls, stream, reps: int = 3) -> float:
+    """Per-call device time of a burst of short launches: the calls are captured once in a CUDA graph and the
+    graph is replayed between two events, so the host's per-call submission cost (the Python binding takes
+    longer to submit a launch than a 20-40 us write takes to run) does not leave the GPU idle between them."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for c in calls:
+            c()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / len(calls))
+    del g
+    return statistics.median(per)
+
+
+def measure_write_burst(w, case, stream, reps: int = 3) -> dict:
+    """Standalone KV write of one workload: a burst of R launches, each from its own source tensors into its
+    own pool pair, so that no launch finds its bytes in L2 (R x bytes >= 4 x L2); per launch = burst / R,
+    replayed from a CUDA graph (graph_burst_ms)."""
+    import torch
+
+    row_bytes = w.num_kv_heads * w.head_dim * (2 if w.dtype != "f32" else 4)
+    tq = int(case.meta.query_start_loc[-1])
+    nbytes = tq * 2 * (2 * row_bytes) + tq * 8
+    n_sets = max(4, min(64, -(-4 * _l2_bytes() // nbytes)))
+    sets = [(case.k_new[0], case.v_new[0], case.k_pools[0], case.v_pools[0])]
+    for _ in range(n_sets - 1):
+        sets.append((case.k_new[0].clone(), case.v_new[0].clone(), torch.empty_like(case.k_pools[0]),
+                     torch.empty_like(case.v_pools[0])))
+    from paged_kv_cache_181_gb300 import _lib
+
+    calls = [lambda k=k, v=v, kp=kp, vp=vp: _lib.paged_kv_write(k, v, case.slots, kp, vp) for k, v, kp, vp in sets]
+    ms = graph_burst_ms(calls, stream, reps)
+    del sets, calls
+    torch.cuda.empty_cache()
+    return {"us_per_launch": ms * 1e3, "algorithmic_bytes_per_launch": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "burst_launches": n_sets, "timing": "burst replayed from one CUDA graph", "row_bytes": row_bytes,
+            "rows": 2 * tq}
+
+
+def measure_workload(name: str, stream, peaks: dict, reps: int = 20) -> dict:
+    """One workload at full size, one layer: the fused write + attention call timed per launch (an L2 flush
+    before each, events around it), its split plan, and the standalone write (measure_write_burst)."""
+    import torch
+
+    from paged_kv_cache_181_gb300 import _lib, configs, workload
+
+    w = configs.ALL[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workload.build_case(w, device=dev, layers=1, data_device=dev)
+    flops = 4 * w.head_dim * w.num_heads * visible_pairs(case.meta)
+    flush = torch.empty(4 * _l2_bytes(), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        case.write_attend(0, stream=stream)
+    torch.cuda.synchronize()
+    plan = _lib.last_split_plan()
+    launches = _lib.last_launches()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            case.write_attend(0, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        wr = measure_write_burst(w, case, stream)
+    del flush
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    tflops = flops / (ms * 1e-3) / 1e12
+    res = {
+        "attention": {"api": "paged_kv_write_attn (fused write + attention), one layer", "ms_per_call": ms,
+                      "algorithmic_flops_per_call": flops, "tflops": tflops,
+                      "frac_of_burst": tflops / peaks["bf16_tflops"],
+                      "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+                      "launches_per_call": launches, "split_plan": {"splits": plan[0], "whole_items": plan[1]},
+                      "l2": "flushed before each timed call", "dtype": w.dtype},
+        "kv_write": wr | {"frac_of_hbm": wr["gbs"] / peaks["hbm_gbs"]},
+        "clocks": clk.summary(),
+    }
+    del case
     torch.cuda.empty_cache()
     return res
 
@@ -734,6 +915,7 @@ def main():
                     help="time the forward as paged_kv_write + paged_attn_varlen per layer (default: the fused call)")
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other API for comparison")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' per-call figures")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

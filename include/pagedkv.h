@@ -74,7 +74,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  * 16-token block.  With PKV_CHECK_BOUNDS a row that breaks the promise is flagged (PKV_DEVERR_BLOCK) and
  * loaded block by block. */
 #define PKV_CONTIGUOUS_KV 0x8u
-/* attention: force n (1..16) key-range splits (needs workspace); 0 = plan automatically */
+/* attention: force n key-range splits (needs workspace); n > 16 is taken as 16; 0 = plan automatically */
 #define PKV_SPLITS(n) ((((uint32_t)(n)) & 0xffu) << 8)
 
 /* Segment modes. */
@@ -283,7 +283,10 @@ PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int m
  *   workspace        device, ws_bytes >= paged_attn_workspace_size(...) when the
  *                    call may split the key range (NULL/0 disables splitting)
  *   max_query_len    >= every row's Sq;  max_seq_len >= every L, <= W * 16
- *   softmax_scale    multiplies Q.K (the pages pass D^-0.5)
+ *   softmax_scale    multiplies Q.K (the pages pass D^-0.5).  For bf16/f16 it must be > 0: the
+ *                    tensor-core kernel requires it, and any other value returns PKV_ERR_UNSUPPORTED
+ *                    unless flags holds PKV_FORCE_SIMT, which runs the CUDA-core kernel (any finite
+ *                    scale, about two orders of magnitude slower).  fp32 takes any finite scale.
  * A query that sees no key (only possible with ill-formed segments) gets 0.
  * Tq == 0, B == 0 or max_query_len == 0: nothing to compute; PKV_OK without a launch
  * (sizes and the dtype are still validated; out is not touched).
@@ -311,8 +314,10 @@ PKV_API pkv_status paged_attn_varlen(const void* q, int64_t Tq, int Hq, const vo
  * a fixed device array of PKV_NOALLOC_SCRATCH_BYTES inside the library, which
  * every GPU that loads the library's device code holds until the process exits.
  * Nothing is allocated at call time.
- *   - The array's device address is looked up once per device, inside the
- *     first call made with that device current; make that first call before
+ *   - The array's device address is looked up once per device and CUDA
+ *     context (a new context on the device, after cudaDeviceReset or a
+ *     caller's own cuCtxCreate, looks it up again), inside the first call
+ *     made with that device and context current; make that first call before
  *     any stream capture.
  *   - All calls share the array and it keeps the last call's contents (nothing
  *     in it has to start at zero).  Calls whose GPU work overlaps -- other

@@ -221,12 +221,46 @@ def _require_metadata(fn: str, *tensors) -> None:
             raise ValueError(f"{fn}: metadata must be int32")
 
 
+def _check_attn_shapes(fn: str, q, key_pool, value_pool, block_table, query_start_loc, seq_lens, segs, seg_start,
+                       out, block_size: int) -> None:
+    """Shapes the C call cannot see: it takes one size per dimension (Tq/Hq/D from q, Hkv and the block
+    count from key_pool, B/W from block_table), so every other tensor must agree with them, or a kernel
+    would read or write past an allocation that no device-side check knows the size of."""
+    if q.dim() != 3 or key_pool.dim() != 3:
+        raise ValueError(f"{fn}: q must be [Tq, Hq, D] and the pools [num_blocks * {block_size}, Hkv, D]")
+    if tuple(value_pool.shape) != tuple(key_pool.shape):
+        raise ValueError(f"{fn}: value_pool shape {tuple(value_pool.shape)} differs from key_pool "
+                         f"{tuple(key_pool.shape)}")
+    if key_pool.shape[2] != q.shape[2]:
+        raise ValueError(f"{fn}: the pools' head dim {key_pool.shape[2]} differs from q's {q.shape[2]}")
+    if key_pool.shape[0] % block_size:
+        raise ValueError(f"{fn}: the pools' {key_pool.shape[0]} slots are not a whole number of {block_size}-slot "
+                         f"blocks")
+    if out is not None and tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"{fn}: out shape {tuple(out.shape)} differs from q {tuple(q.shape)}")
+    if block_table.dim() != 2:
+        raise ValueError(f"{fn}: block_table must be [B, W]")
+    B = block_table.shape[0]
+    if query_start_loc.numel() != B + 1 or seq_lens.numel() != B:
+        raise ValueError(f"{fn}: query_start_loc must hold B+1 = {B + 1} and seq_lens B = {B} entries "
+                         f"(got {query_start_loc.numel()} and {seq_lens.numel()})")
+    if (segs is None) != (seg_start is None):
+        raise ValueError(f"{fn}: segs and seg_start go together")
+    if segs is not None:
+        if segs.dim() != 2 or segs.shape[1] != 4:
+            raise ValueError(f"{fn}: segs must be [n, 4] (q_start, q_end, kv_end, mode)")
+        if seg_start.numel() != B + 1:
+            raise ValueError(f"{fn}: seg_start must hold B+1 = {B + 1} entries (got {seg_start.numel()})")
+
+
 def paged_kv_write(k, v, slot_mapping, key_pool, value_pool, *, flags: int = 0, stream=None) -> None:
     """key_pool[slot[t]] = k[t]; value_pool[slot[t]] = v[t] (pools ``[num_slots, Hkv, D]``)."""
     T, hkv, d = k.shape
-    _require("paged_kv_write", k, v, slot_mapping, key_pool, value_pool)
     if v.shape != k.shape or key_pool.shape != value_pool.shape or key_pool.shape[1:] != k.shape[1:]:
         raise ValueError("paged_kv_write: shape mismatch")
+    if slot_mapping.numel() != T:
+        raise ValueError("paged_kv_write: slot_mapping must hold one slot per token")
+    _require("paged_kv_write", k, v, slot_mapping, key_pool, value_pool)
     if k.dtype != key_pool.dtype or v.dtype != value_pool.dtype or k.dtype != v.dtype:
         raise ValueError("paged_kv_write: sources and pools must share one dtype")
     if slot_mapping.dtype != _torch().int64 or slot_mapping.numel() != T:
@@ -264,6 +298,8 @@ def paged_attn_varlen(q, key_pool, value_pool, block_table, query_start_loc, seq
                       workspace=None, flags: int = 0, block_size: int = 16, stream=None):
     """Paged varlen attention; pools are ``[num_blocks * 16, Hkv, D]``; returns ``out``."""
     torch = _torch()
+    _check_attn_shapes("paged_attn_varlen", q, key_pool, value_pool, block_table, query_start_loc, seq_lens, segs,
+                       seg_start, out, block_size)
     Tq, hq, d = q.shape
     hkv = key_pool.shape[1]
     if out is None:
@@ -288,19 +324,21 @@ def paged_kv_write_attn(q, k, v, slot_mapping, key_pool, value_pool, block_table
                         out=None, workspace=None, flags: int = 0, block_size: int = 16, stream=None):
     """paged_kv_write + paged_attn_varlen in one launch (see include/pagedkv.h); returns ``out``."""
     torch = _torch()
+    _check_attn_shapes("paged_kv_write_attn", q, key_pool, value_pool, block_table, query_start_loc, seq_lens, segs,
+                       seg_start, out, block_size)
     Tq, hq, d = q.shape
     hkv = key_pool.shape[1]
     if out is None:
         out = torch.empty_like(q)
+    if k.shape != (Tq, hkv, d) or v.shape != k.shape:
+        raise ValueError("paged_kv_write_attn: k and v must be [Tq, Hkv, D]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != Tq:
+        raise ValueError("paged_kv_write_attn: slot_mapping must be int64 [Tq]")
     _require("paged_kv_write_attn", q, k, v, slot_mapping, key_pool, value_pool, block_table, query_start_loc, seq_lens,
              segs, seg_start, out, workspace)
     _require_metadata("paged_kv_write_attn", block_table, query_start_loc, seq_lens, segs, seg_start)
     if len({q.dtype, k.dtype, v.dtype, key_pool.dtype, value_pool.dtype, out.dtype}) != 1:
         raise ValueError("paged_kv_write_attn: q, k, v, pools and out must share one dtype")
-    if k.shape != (Tq, hkv, d) or v.shape != k.shape:
-        raise ValueError("paged_kv_write_attn: k and v must be [Tq, Hkv, D]")
-    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != Tq:
-        raise ValueError("paged_kv_write_attn: slot_mapping must be int64 [Tq]")
     B, W = block_table.shape
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ok(lib.paged_kv_write_attn(_dptr(q), _dptr(k), _dptr(v), _dptr(slot_mapping), Tq, hq, _dptr(key_pool),
@@ -319,6 +357,8 @@ def paged_attn_varlen_noalloc(q, key_pool, value_pool, block_table, query_start_
     For callers that cannot allocate device memory; see include/pagedkv.h.
     """
     torch = _torch()
+    _check_attn_shapes("paged_attn_varlen_noalloc", q, key_pool, value_pool, block_table, query_start_loc, seq_lens,
+                       segs, seg_start, out, block_size)
     Tq, hq, d = q.shape
     hkv = key_pool.shape[1]
     if out is None:

@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -35,7 +36,7 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _run(cmd: list[str], verbose: bool) -> None:
+def _run(cmd: list[str], verbose: bool, log: str | None = None) -> str:
     if verbose:
         print(" ".join(cmd), flush=True)
     res = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
@@ -43,6 +44,50 @@ def _run(cmd: list[str], verbose: bool) -> None:
         print(res.stdout, flush=True)
     if res.returncode != 0:
         raise RuntimeError(f"build step failed ({res.returncode}): {' '.join(cmd)}\n{res.stdout}")
+    if log:
+        with open(log, "w") as f:
+            f.write(res.stdout)
+    return res.stdout
+
+
+# The tensor-core attention kernel hands registers between its warpgroups with setmaxnreg, a split
+# sized for exactly the register count the kernel is compiled to; that count is checked here, from
+# ptxas's report, so that a toolchain which allocates differently fails the build instead of every
+# bf16/f16 call at run time (the launcher keeps the same check as a backstop).
+TC_SOURCE = "attn_tc.cu"
+TC_KERNEL = "attn_tc_kernel"
+
+
+def expected_tc_registers(source: str) -> int:
+    m = re.search(r"constexpr\s+int\s+kLaunchRegs\s*=\s*(\d+)", source)
+    if not m:
+        raise RuntimeError(f"{TC_SOURCE}: kLaunchRegs not found")
+    return int(m.group(1))
+
+
+def check_tc_registers(ptxas_log: str, expected: int) -> int:
+    """Every instantiation of the tensor-core kernel in a ``-Xptxas -v`` log uses ``expected`` registers;
+    returns how many instantiations were checked, raises RuntimeError otherwise."""
+    seen = 0
+    current = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current is not None:
+            if TC_KERNEL in current:
+                seen += 1
+                if int(m.group(1)) != expected:
+                    raise RuntimeError(
+                        f"{TC_SOURCE}: {current} compiled to {m.group(1)} registers per thread, but its warpgroup "
+                        f"register split (setmaxnreg) is sized for {expected}; adjust kLaunchRegs/kRegsLow/"
+                        f"kRegsHigh or the kernel's register use")
+            current = None
+    if seen == 0:
+        raise RuntimeError(f"{TC_SOURCE}: no register report for {TC_KERNEL} in the ptxas output")
+    return seen
 
 
 def _stale(obj: str, deps: list[str]) -> bool:
@@ -60,27 +105,37 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
     headers.append(os.path.join(INCLUDE, "pagedkv.h"))
     jobs = []
     objs = []
+    tc_log = os.path.join(OUT_DIR, TC_SOURCE + ".ptxas.txt")
     for src in CUDA_SOURCES:
         path = os.path.join(CSRC, src)
         obj = os.path.join(OUT_DIR, src + ".o")
         objs.append(obj)
-        if force or _stale(obj, [path, *headers]):
+        is_tc = src == TC_SOURCE
+        if force or _stale(obj, [path, *headers]) or (is_tc and _stale(tc_log, [obj])):
             cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                    "-I", INCLUDE, "-I", CSRC, "-c", path, "-o", obj]
-            if ptxas_verbose:
+            if ptxas_verbose or is_tc:
                 cmd += ["-Xptxas", "-v"]
-            jobs.append(cmd)
+            jobs.append((cmd, tc_log if is_tc else None))
     for src in HOST_SOURCES:
         path = os.path.join(CSRC, src)
         obj = os.path.join(OUT_DIR, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path, *headers]):
-            jobs.append(["g++", "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC, "-c",
-                         path, "-o", obj])
+            jobs.append((["g++", "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC, "-c",
+                          path, "-o", obj], None))
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
-            for f in [ex.submit(_run, cmd, verbose) for cmd in jobs]:
+            for f in [ex.submit(_run, cmd, verbose, log) for cmd, log in jobs]:
                 f.result()
+    with open(os.path.join(CSRC, TC_SOURCE)) as f:
+        expected = expected_tc_registers(f.read())
+    with open(tc_log) as f:
+        try:
+            check_tc_registers(f.read(), expected)
+        except RuntimeError:
+            os.remove(tc_log)  # the next build compiles the kernel again
+            raise
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + ".tmp"
         _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"], verbose)

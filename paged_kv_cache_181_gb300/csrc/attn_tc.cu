@@ -758,11 +758,13 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
   }
   const size_t smem = sizeof(TcSmem<D>) + 1024;
   // Per device, once; racing first calls from several host threads only repeat the same settings.
-  static std::atomic<bool> attr_set[64];
+  // Keyed on the context: function attributes belong to the context they were set in.
+  static std::atomic<uint64_t> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   const bool cached = dev >= 0 && dev < 64;
-  if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
+  const uint64_t ctx = pkv_context_id();
+  if (!cached || ctx == 0 || attr_set[dev].load(std::memory_order_acquire) != ctx) {
     // The warpgroup register split is only valid for the register count it was sized for.
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, BF16>);
@@ -770,7 +772,7 @@ int launch_tc(const PkvAttnArgs& a, cudaStream_t s) {
     if (fa.numRegs != kLaunchRegs) return (int)cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(attn_tc_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    if (cached) attr_set[dev].store(true, std::memory_order_release);
+    if (cached) attr_set[dev].store(ctx, std::memory_order_release);
   }
   const int g = a.Hq / a.Hkv;
   const int n_qp = (a.max_query_len + 2 * BM - 1) / (2 * BM);

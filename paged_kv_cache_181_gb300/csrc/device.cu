@@ -1,6 +1,7 @@
 // Device entry points of libpagedkv: argument validation, key-range split
 // planning, launches, and the device error word read back by pkv_check().
 
+#include <cuda.h>
 #include <math.h>
 
 #include <mutex>
@@ -14,6 +15,7 @@ __device__ unsigned int g_pkv_error_word;
 
 constexpr int kMaxDevices = 64;
 unsigned int* g_err_ptr[kMaxDevices] = {};
+uint64_t g_err_ctx[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::mutex g_mu;
 
@@ -25,19 +27,45 @@ int current_device() {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = kPkvMaxSplits;
 constexpr int kWorkspaceSplits = 8;  // paged_attn_workspace_size covers at least this many (forced splits)
 
 }  // namespace
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+uint64_t pkv_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (CtxGetCurrentFn)p;
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (CtxGetIdFn)p;
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return (uint64_t)id;
+}
 
 unsigned int* pkv_device_error_word() {
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_err_ptr[dev]) {
+  const uint64_t ctx = pkv_context_id();
+  if (!g_err_ptr[dev] || ctx == 0 || g_err_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return nullptr;
     g_err_ptr[dev] = (unsigned int*)p;
+    g_err_ctx[dev] = pkv_context_id();  // the lookup makes the device's primary context current
   }
   return g_err_ptr[dev];
 }
@@ -89,9 +117,8 @@ extern "C" pkv_status paged_kv_write(const void* k, const void* v, const int64_t
                     (long long)row_bytes);
   if (row_bytes / 16 > (1 << 30)) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_kv_write: row too large");
   const int check = (flags & PKV_CHECK_BOUNDS) ? 1 : 0;
-  // The error word is always passed: the staged copy reports wait timeouts through it.
-  unsigned int* err = pkv_device_error_word();
-  if (!err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: device error word unavailable");
+  unsigned int* err = check ? pkv_device_error_word() : nullptr;
+  if (check && !err) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: device error word unavailable");
   const int rc = pkv_launch_kv_write(k, v, slot_mapping, T, key_pool, value_pool, num_slots, (int)row_bytes, err,
                                      check, stream);
   if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "paged_kv_write: launch failed: %s", cudaGetErrorString((cudaError_t)rc));
@@ -223,6 +250,12 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
   if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16)
     return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dt);
   if (!isfinite(softmax_scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: softmax_scale is not finite", fn);
+  // The tensor-core kernel keeps its running maximum for a positive scale only; the CUDA-core kernel,
+  // two orders of magnitude slower, takes any scale, but only when asked for by name.
+  if (dt != PKV_F32 && !(softmax_scale > 0.f) && !(flags & PKV_FORCE_SIMT))
+    return pkv_fail(PKV_ERR_UNSUPPORTED,
+                    "%s: a bf16/f16 call needs softmax_scale > 0 (got %g); pass PKV_FORCE_SIMT to run it on the "
+                    "CUDA-core kernel", fn, (double)softmax_scale);
   if ((int64_t)max_seq_len > (int64_t)W * block_size)
     return pkv_fail(PKV_ERR_INVALID_ARG, "%s: max_seq_len %d exceeds the table's %d x %d slots", fn,
                     max_seq_len, W, block_size);

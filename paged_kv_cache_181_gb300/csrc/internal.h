@@ -17,6 +17,15 @@ unsigned int* pkv_device_error_word();
 
 inline int pkv_dtype_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
 
+// Most key-range splits per item; larger PKV_SPLITS(n) requests are clamped to it.
+constexpr int kPkvMaxSplits = 16;
+
+// Process-unique id of the CUDA context current on this thread (0: none, or the driver call is
+// unavailable).  Per-device caches of device addresses and function attributes are keyed on it, so
+// that a new context on the same device (after cudaDeviceReset, or a caller's own context) looks
+// them up again instead of reusing the old context's values.
+uint64_t pkv_context_id();
+
 // Per-row work description shared by the attention kernels.
 struct PkvAttnArgs {
   const void* q;

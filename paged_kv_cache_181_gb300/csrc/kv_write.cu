@@ -3,104 +3,90 @@
 // video and the action tokens).
 //
 // HBM-bound copy of whole rows: a token's K (or V) row is Hkv*D*elem contiguous
-// bytes both in the source and at its pool slot.  The copy engine moves them:
-// one warp per CTA, whose lane 0 takes batches of kStages rows, loads each row
-// into shared memory with one bulk copy (completion counted on the row's
-// mbarrier) and writes it to its slot with one bulk store; the next batch
-// reuses the buffers once the stores have read them.  Grid: up to kCtasPerSm
-// CTAs per SM.  Measured on the long-window workload (3120 tokens x 10 KB rows,
-// K and V): 23.6 us per launch in 40-launch bursts (80 % of the measured copy
-// bandwidth), against 25.3 us for one warp per row with 8 16-byte loads in
-// flight per lane -- which stays as the kernel for rows too wide to stage.
-
-#include <atomic>
+// bytes both in the source and at its pool slot.  The rows are cut into chunks
+// of kChunkVecs 16-byte vectors (2 KB); a warp copies one chunk per step, each
+// lane loading its kU vectors before storing any, and the warps walk the flat
+// list of (row, chunk) pairs with a grid stride, so every warp of a full wave
+// has work even when the rows are few and wide (the long-window workload has
+// 6240 rows of 10 KB for 152 x 48 warps).  Grid: one wave of resident CTAs.
+// Measured against other designs on the workloads' shapes, in bursts of
+// launches on distinct buffers (per launch, % of the measured copy bandwidth):
+//   rows of 6 KB (201 MB): 34.5 us = 86 %; rows of 10 KB (128 MB): 23.0 us =
+//   82 %; rows of 2 KB (52 MB): 12.4 us = 61 %; rows of 3 KB (38 MB): 10.3 us
+//   = 55 % (the small launches pay a fixed ~4-5 us of ramp-up and drain).
+// One warp per whole row, all of it in registers, measured the same; TMA bulk
+// copies staged through shared memory were slower (one issuing thread per CTA
+// waits on each store's shared-memory read: 35-55 % with one CTA per SM, 78-85 %
+// with four).
 
 #include "kv_copy.cuh"
-#include "tc_ptx.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 4;         // rows in flight per CTA
-constexpr int kCtasPerSm = 4;
-constexpr int kMaxStageBytes = 200 * 1024;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr int kU = 4;                       // vectors in flight per lane
+constexpr int kChunkVecs = 32 * kU;         // 2 KB per warp step
 
-PKV_DEVINLINE void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(ptx::smem_u32(bar))
-               : "memory");
-}
-
-PKV_DEVINLINE void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
-}
-
-// Rows are (token, K|V) pairs: row r is K (r even) or V (r odd) of token r/2.  A negative slot skips
-// the token; with `check`, slots >= num_slots are flagged and skipped.  Every wait is bounded: on
-// expiry the CTA records PKV_DEVERR_TIMEOUT, waits for its stores and exits.
-__global__ void __launch_bounds__(32) kv_write_bulk_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
-                                                            const int64_t* __restrict__ slots, int64_t T,
-                                                            uint8_t* __restrict__ kp, uint8_t* __restrict__ vp,
-                                                            int64_t num_slots, int row_bytes, unsigned int* err,
-                                                            int check) {
-  extern __shared__ __align__(128) uint8_t stage[];
-  __shared__ uint64_t bar[kStages];
-  if (threadIdx.x != 0) return;
-  for (int s = 0; s < kStages; ++s) ptx::mbar_init(&bar[s], 1);
-  ptx::fence_mbar_init();
-  const uint32_t sbase = ptx::smem_u32(stage);
-  const int64_t rows = 2 * T;
-  int never = 0;
-  uint32_t phase = 0;
-  for (int64_t b0 = (int64_t)blockIdx.x * kStages; b0 < rows; b0 += (int64_t)gridDim.x * kStages, phase ^= 1) {
-    int64_t dst[kStages];
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      const int64_t r = b0 + s;
-      dst[s] = -1;
-      if (r < rows) {
-        const int64_t sl = __ldg(slots + (r >> 1));
-        if (sl >= 0 && check && sl >= num_slots) pkv_raise(err, PKV_DEVERR_SLOT);
-        else dst[s] = sl;
-      }
-      // Each stage's barrier completes once per batch: on its row's bytes, or at once when it has none.
-      if (dst[s] >= 0) {
-        ptx::mbar_arrive_expect_tx(&bar[s], (uint32_t)row_bytes);
-        bulk_load(sbase + s * row_bytes, ((r & 1) ? v : k) + (r >> 1) * row_bytes, (uint32_t)row_bytes, &bar[s]);
-      } else {
-        ptx::mbar_arrive(&bar[s]);
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      if (!ptx::mbar_wait(&bar[s], phase, &never, kWaitLimitNs)) {
-        pkv_raise(err, PKV_DEVERR_TIMEOUT);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        return;
-      }
-      if (dst[s] >= 0) {
-        const int64_t r = b0 + s;
-        bulk_store(((r & 1) ? vp : kp) + dst[s] * row_bytes, sbase + s * row_bytes, (uint32_t)row_bytes);
-      }
-    }
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the buffers are free again
-  }
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Rows too wide to stage: one warp per row (pkv_scatter).
+// Rows are (token, K|V) pairs: row r is K (r even) or V (r odd) of token r/2; chunk c of the flat
+// list is chunk c % cpr of row c / cpr.  A negative slot skips the token; with `check`, slots >=
+// num_slots are flagged and skipped.  I is the index type: 32-bit when every chunk index fits.
+template <typename I>
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                             const int64_t* __restrict__ slots, int64_t T,
                                                             uint4* __restrict__ kp, uint4* __restrict__ vp,
-                                                            int64_t num_slots, int vec_per_row, unsigned int* err,
-                                                            int check) {
-  pkv_scatter(k, v, slots, T, kp, vp, num_slots, vec_per_row, err, check,
-              (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5), (int64_t)gridDim.x * kWarps, threadIdx.x & 31,
-              nullptr);
+                                                            int64_t num_slots, int vec_per_row, int cpr,
+                                                            unsigned int* err, int check) {
+  const int lane = threadIdx.x & 31;
+  const I n = (I)(2 * T) * (I)cpr;
+  const I stride = (I)gridDim.x * kWarps;
+  for (I c = (I)blockIdx.x * kWarps + (threadIdx.x >> 5); c < n; c += stride) {
+    const I row = c / (I)cpr;
+    const int ci = (int)(c - row * (I)cpr);
+    const int64_t t = (int64_t)(row >> 1);
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) continue;
+    if (check && s >= num_slots) {
+      if (lane == 0 && ci == 0) pkv_raise(err, PKV_DEVERR_SLOT);
+      continue;
+    }
+    const uint4* src = ((row & 1) ? v : k) + t * vec_per_row;
+    uint4* dst = ((row & 1) ? vp : kp) + s * vec_per_row;
+    const int base = ci * kChunkVecs + lane;
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (base + 32 * u < vec_per_row) x[u] = __ldcs(src + base + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (base + 32 * u < vec_per_row) dst[base + 32 * u] = x[u];
+  }
+}
+
+// Resident CTAs per SM of one instantiation, per device (queried once).
+template <typename I>
+int resident_ctas() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_write_kernel<I>, kThreads, 0) != cudaSuccess || n <= 0) n = 4;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+template <typename I>
+int launch_write(const void* k, const void* v, const int64_t* slots, int64_t T, void* kp, void* vp, int64_t num_slots,
+                 int vec_per_row, int cpr, unsigned int* err, int check, int sms, void* stream) {
+  const int64_t chunks = 2 * T * (int64_t)cpr;
+  int64_t grid = (chunks + kWarps - 1) / kWarps;
+  const int64_t cap = (int64_t)sms * resident_ctas<I>();
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  kv_write_kernel<I><<<(unsigned)grid, kThreads, 0, (cudaStream_t)stream>>>(
+      (const uint4*)k, (const uint4*)v, slots, T, (uint4*)kp, (uint4*)vp, num_slots, vec_per_row, cpr, err, check);
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -109,35 +95,12 @@ int pkv_launch_kv_write(const void* k, const void* v, const int64_t* slots, int6
                         int64_t num_slots, int row_bytes, unsigned int* err, int check, void* stream) {
   int sms = pkv_sm_count();
   if (sms <= 0) sms = 152;
-  const int64_t smem = (int64_t)kStages * row_bytes;
-  if (smem <= kMaxStageBytes && err) {
-    // Per device, once; racing first calls from several host threads only repeat the same setting.
-    static std::atomic<bool> attr_set[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const bool cached = dev >= 0 && dev < 64;
-    if (!cached || !attr_set[dev].load(std::memory_order_acquire)) {
-      const cudaError_t e = cudaFuncSetAttribute(kv_write_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kMaxStageBytes);
-      if (e != cudaSuccess) return (int)e;
-      if (cached) attr_set[dev].store(true, std::memory_order_release);
-    }
-    int64_t grid = (2 * T + kStages - 1) / kStages;
-    const int64_t cap = (int64_t)sms * kCtasPerSm;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    kv_write_bulk_kernel<<<(unsigned)grid, 32, (size_t)smem, (cudaStream_t)stream>>>(
-        (const uint8_t*)k, (const uint8_t*)v, slots, T, (uint8_t*)kp, (uint8_t*)vp, num_slots, row_bytes, err, check);
-    return (int)cudaGetLastError();
-  }
   const int vec_per_row = row_bytes / 16;
-  int64_t grid = (T * 2 + kWarps - 1) / kWarps;  // one warp per row
-  const int64_t cap = (int64_t)sms * 8;           // 8 resident 256-thread CTAs per SM
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  kv_write_kernel<<<(unsigned)grid, kThreads, 0, (cudaStream_t)stream>>>(
-      (const uint4*)k, (const uint4*)v, slots, T, (uint4*)kp, (uint4*)vp, num_slots, vec_per_row, err, check);
-  return (int)cudaGetLastError();
+  const int cpr = (vec_per_row + kChunkVecs - 1) / kChunkVecs;
+  // 32-bit chunk indices while c + stride cannot wrap (the stride is at most a few hundred thousand).
+  if (2 * T * (int64_t)cpr < ((int64_t)1 << 31))
+    return launch_write<uint32_t>(k, v, slots, T, kp, vp, num_slots, vec_per_row, cpr, err, check, sms, stream);
+  return launch_write<int64_t>(k, v, slots, T, kp, vp, num_slots, vec_per_row, cpr, err, check, sms, stream);
 }
 
 // ---------------------------------------------------------------- block gather into staging

@@ -14,10 +14,12 @@
 // Every GPU on which this library's device code is loaded holds it until the
 // process exits.  In host code the array's name is only a host-side stand-in,
 // not a device address, so its device address is looked up once per device
-// (with that device current) through cudaGetSymbolAddress and cached; that
-// happens inside the first call made on each device, which should therefore
-// come before any stream capture.  All calls share the one array and it keeps
-// whatever the last call left in it; nothing in it needs to start at zero
+// (with that device current) through cudaGetSymbolAddress and cached, keyed
+// on the current CUDA context, so a new context on the device (after
+// cudaDeviceReset, or a caller's own context) looks it up again; that happens
+// inside the first call made on each device (and in each new context), which
+// should therefore come before any stream capture.  All calls share the one
+// array and it keeps whatever the last call left in it; nothing in it needs to start at zero
 // (every split writes its whole partial output and log-sum-exp before the
 // combine reads them).  Calls whose work overlaps on the GPU -- on different
 // streams, or from different host threads without ordering -- race on the
@@ -33,22 +35,25 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
+uint64_t g_scratch_ctx[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device (looked up once per device and context).
 pkv_status scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return pkv_fail(PKV_ERR_UNSUPPORTED, "paged_attn_varlen_noalloc: device %d", dev);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  const uint64_t ctx = pkv_context_id();
+  if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return pkv_fail(PKV_ERR_CUDA, "paged_attn_varlen_noalloc: cudaGetSymbolAddress of the scratch array failed: %s",
                       cudaGetErrorString(e));
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = pkv_context_id();
   }
   *out = g_scratch_addr[dev];
   return PKV_OK;
@@ -66,7 +71,9 @@ extern "C" pkv_status paged_attn_varlen_noalloc(const void* q, int64_t Tq, int H
   pkv_clear_error();
   pkv_set_launches(0);
   // A forced number of splits that the fixed scratch cannot hold is refused before anything runs.
-  const int forced = (int)((flags >> 8) & 0xffu);
+  // (Clamped as paged_attn_varlen clamps it, so both calls accept the same requests.)
+  int forced = (int)((flags >> 8) & 0xffu);
+  if (forced > kPkvMaxSplits) forced = kPkvMaxSplits;
   if (forced > 1 && Tq > 0 && Hq > 0 && D > 0) {
     const unsigned long long need =
         (unsigned long long)forced * (unsigned long long)Tq * (unsigned long long)Hq * ((unsigned long long)D + 1) * 4ull;

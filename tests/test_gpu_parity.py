@@ -160,7 +160,7 @@ def _tail_workload():
                                pool_blocks=4096, seed=51)
 
 
-def _run_tail(lib, w, fused, workspace_splits=None, scale_sign=1.0):
+def _run_tail(lib, w, fused, workspace_splits=None, scale_sign=1.0, flags=0):
     from paged_kv_cache_181_gb300 import workload
 
     case = workload.build_case(w, poison=True, keep_draws=True, layers=1)
@@ -169,10 +169,10 @@ def _run_tail(lib, w, fused, workspace_splits=None, scale_sign=1.0):
         case.workspace = case.workspace[: workspace_splits * tq * w.num_heads * (w.head_dim + 1) * 4]
     case.scale *= scale_sign
     if fused:
-        out = case.write_attend(0, flags=lib.PKV_CHECK_BOUNDS)
+        out = case.write_attend(0, flags=lib.PKV_CHECK_BOUNDS | flags)
     else:
         case.write(0, lib.PKV_CHECK_BOUNDS)
-        out = case.attend(0, lib.PKV_CHECK_BOUNDS)
+        out = case.attend(0, lib.PKV_CHECK_BOUNDS | flags)
     launches, plan = lib.last_launches(), lib.last_split_plan()
     torch.cuda.synchronize()
     assert lib.check() == 0
@@ -204,7 +204,16 @@ def test_split_tail_shrinks_to_the_workspace(lib):
 
 
 def test_negative_scale_plans_for_the_kernel_that_runs(lib):
-    """A negative softmax scale runs on the CUDA-core kernel, whose split plan has no whole items."""
+    """A negative softmax scale on bf16 is refused unless the CUDA-core kernel is asked for by name; then it
+    runs there, with that kernel's split plan (no whole items), and matches the oracle."""
+    from paged_kv_cache_181_gb300 import workload
+
     w = _tail_workload()
-    launches, (splits, whole) = _run_tail(lib, w, False, scale_sign=-1.0)
+    case = workload.build_case(w, layers=1)
+    case.scale = -case.scale
+    with pytest.raises(lib.PkvError) as e:
+        case.attend(0)
+    assert e.value.status == lib.PKV_ERR_UNSUPPORTED and lib.last_launches() == 0
+    del case
+    launches, (splits, whole) = _run_tail(lib, w, False, scale_sign=-1.0, flags=lib.PKV_FORCE_SIMT)
     assert whole == 0, (splits, whole)

@@ -207,3 +207,52 @@ def test_wrappers_refuse_host_tensors(lib):
     for call in calls:
         with pytest.raises(ValueError, match="CUDA device"):
             call()
+
+
+def test_attention_wrappers_refuse_mismatched_shapes(lib):
+    # The C call takes one size per dimension (D from q, Hkv and the block count from key_pool, B from the
+    # table): a tensor that disagrees with them would send a kernel past its allocation, so the binding stops
+    # it before the C call (and before it looks at the device).
+    import torch
+
+    bf = torch.bfloat16
+    q = torch.zeros(4, 4, 64, dtype=bf)
+    pool = torch.zeros(64, 2, 64, dtype=bf)
+    k = torch.zeros(4, 2, 64, dtype=bf)
+    slots = torch.arange(4, dtype=torch.int64)
+    qsl = torch.tensor([0, 4], dtype=torch.int32)
+    seq = torch.tensor([4], dtype=torch.int32)
+    table = torch.zeros(1, 4, dtype=torch.int32)
+    segs = torch.zeros(1, 4, dtype=torch.int32)
+    seg_start = torch.tensor([0, 1], dtype=torch.int32)
+    good = dict(q=q, kp=pool, vp=pool, table=table, qsl=qsl, seq=seq, segs=segs, seg_start=seg_start, out=None)
+    bad = [
+        ("value_pool shape", dict(vp=torch.zeros(48, 2, 64, dtype=bf))),
+        ("head dim", dict(kp=torch.zeros(64, 2, 128, dtype=bf), vp=torch.zeros(64, 2, 128, dtype=bf))),
+        ("whole number", dict(kp=torch.zeros(60, 2, 64, dtype=bf), vp=torch.zeros(60, 2, 64, dtype=bf))),
+        ("out shape", dict(out=torch.zeros(3, 4, 64, dtype=bf))),
+        ("B\\+1", dict(qsl=torch.tensor([0, 2, 4], dtype=torch.int32))),
+        ("B\\+1", dict(seq=torch.tensor([4, 4], dtype=torch.int32))),
+        ("seg_start", dict(seg_start=torch.tensor([0, 1, 1], dtype=torch.int32))),
+        ("segs must be", dict(segs=torch.zeros(4, dtype=torch.int32))),
+        ("go together", dict(seg_start=None)),
+        ("q must be", dict(q=torch.zeros(4, 256, dtype=bf))),
+    ]
+    for what, change in bad:
+        a = good | change
+        calls = [
+            lambda: lib.paged_attn_varlen(a["q"], a["kp"], a["vp"], a["table"], a["qsl"], a["seq"], 4, 64, 0.125,
+                                          segs=a["segs"], seg_start=a["seg_start"], out=a["out"]),
+            lambda: lib.paged_attn_varlen_noalloc(a["q"], a["kp"], a["vp"], a["table"], a["qsl"], a["seq"], 4, 64,
+                                                  0.125, segs=a["segs"], seg_start=a["seg_start"], out=a["out"]),
+            lambda: lib.paged_kv_write_attn(a["q"], k, k, slots, a["kp"], a["vp"], a["table"], a["qsl"], a["seq"], 4,
+                                            64, 0.125, segs=a["segs"], seg_start=a["seg_start"], out=a["out"]),
+        ]
+        for call in calls:
+            with pytest.raises(ValueError, match=what):
+                call()
+    # The same call with consistent shapes gets as far as the device check.
+    with pytest.raises(ValueError, match="CUDA device"):
+        lib.paged_attn_varlen(q, pool, pool, table, qsl, seq, 4, 64, 0.125, segs=segs, seg_start=seg_start)
+    with pytest.raises(ValueError, match="one slot per token"):
+        lib.paged_kv_write(k, k, torch.arange(3, dtype=torch.int64), pool, pool)

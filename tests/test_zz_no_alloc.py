@@ -3,20 +3,23 @@
 Such callers (fixed device-memory arenas, real-time loops that must not
 allocate, plugin hosts without an allocator) call paged_attn_varlen_noalloc,
 which takes no workspace and keeps its split-KV partial results in a fixed
-scratch array inside the library.  Its results must match paged_attn_varlen
-(given its own workspace) within the tolerance used elsewhere in these tests,
-call after call, whatever the previous call left in the shared scratch.
+scratch array inside the library.  Its results must match the float64 oracle
+within the tolerances used elsewhere in these tests, and be bit-identical to
+paged_attn_varlen given its own workspace when both calls run the same split
+plan -- call after call, whatever the previous call left in the shared scratch.
 
 This file is named so that pytest collects it last.
 """
-
-import ctypes as C
 
 import numpy as np
 import pytest
 import torch
 
+from oracle import pagedattn as pa
+
 pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: (1e-4, 1e-4), torch.bfloat16: (2e-2, 2e-3), torch.float16: (2e-2, 2e-3)}
 
 
 @pytest.fixture(scope="module")
@@ -27,36 +30,55 @@ def lib():
 
 
 def make_case(seed, dtype, hq, hkv, d, sq, kv, spans):
-    """Random pools and a shuffled table; per-row segments from the library's build_segments."""
+    """Random pools and a shuffled table; per-row segments from the library's build_segments for the GPU
+    calls and from the oracle's for the oracle (the two are compared bit for bit elsewhere)."""
     from paged_kv_cache_181_gb300 import _lib
 
     g = torch.Generator().manual_seed(seed)
     B = len(sq)
     W = max(-(-L // 16) for L in kv) + 1
     nblk = B * W + 4
-    q = torch.randn(sum(sq), hq, d, generator=g).to(dtype).cuda()
-    kp = torch.randn(nblk * 16, hkv, d, generator=g).to(dtype).cuda()
-    vp = torch.randn(nblk * 16, hkv, d, generator=g).to(dtype).cuda()
-    table = torch.randperm(nblk, generator=g)[: B * W].reshape(B, W).to(torch.int32).cuda()
-    qsl = torch.tensor(np.concatenate([[0], np.cumsum(sq)]), dtype=torch.int32).cuda()
-    seq = torch.tensor(kv, dtype=torch.int32).cuda()
+    q = torch.randn(sum(sq), hq, d, generator=g).to(dtype)
+    kp = torch.randn(nblk * 16, hkv, d, generator=g).to(dtype)
+    vp = torch.randn(nblk * 16, hkv, d, generator=g).to(dtype)
+    table = torch.randperm(nblk, generator=g)[: B * W].reshape(B, W).to(torch.int32)
+    qsl = np.concatenate([[0], np.cumsum(sq)]).astype(np.int32)
     rows = [_lib.build_segments(spans[b], kv[b] - sq[b], sq[b], kv[b]) for b in range(B)]
-    segs = torch.tensor([s for r in rows for s in r], dtype=torch.int32).reshape(-1, 4).cuda()
-    seg_start = torch.tensor(np.concatenate([[0], np.cumsum([len(r) for r in rows])]), dtype=torch.int32).cuda()
-    return dict(q=q, kp=kp, vp=vp, table=table, qsl=qsl, seq=seq, segs=segs, seg_start=seg_start,
-                max_q=max(sq), max_kv=W * 16)
+    segs = torch.tensor([s for r in rows for s in r], dtype=torch.int32).reshape(-1, 4)
+    seg_start = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    oracle = dict(q=q.float().numpy(), kp=kp.float().numpy(), vp=vp.float().numpy(), table=table.numpy().astype(np.int64),
+                  qsl=qsl.astype(np.int64), seq=np.array(kv, dtype=np.int64),
+                  segments=[pa.build_segments(spans[b], kv[b] - sq[b], sq[b]) for b in range(B)])
+    return dict(q=q.cuda(), kp=kp.cuda(), vp=vp.cuda(), table=table.cuda(), qsl=torch.from_numpy(qsl).cuda(),
+                seq=torch.tensor(kv, dtype=torch.int32).cuda(), segs=segs.cuda(),
+                seg_start=torch.from_numpy(seg_start).cuda(), max_q=max(sq), max_kv=W * 16, oracle=oracle)
 
 
 def run_both(lib, c, flags):
-    ws = torch.empty(lib.workspace_size(c["q"].shape[0], c["q"].shape[1], c["q"].shape[2], 1, 1, 1),
-                     dtype=torch.uint8, device="cuda")
-    args = (c["q"], c["kp"], c["vp"], c["table"], c["qsl"], c["seq"], c["max_q"], c["max_kv"], c["q"].shape[2] ** -0.5)
+    """The workspace call, then the allocation-free call, on the same inputs; outputs, launches and plans."""
+    tq, hq, d = c["q"].shape
+    B = c["table"].shape[0]
+    # Room for the most splits either call runs (16), so the workspace never shrinks the plan.
+    nbytes = max(lib.workspace_size(tq, hq, d, B, c["max_q"], c["max_kv"]), 16 * tq * hq * (d + 1) * 4)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    args = (c["q"], c["kp"], c["vp"], c["table"], c["qsl"], c["seq"], c["max_q"], c["max_kv"], d ** -0.5)
     ref = lib.paged_attn_varlen(*args, segs=c["segs"], seg_start=c["seg_start"], workspace=ws, flags=flags)
+    ref_plan = lib.last_split_plan()
     got = lib.paged_attn_varlen_noalloc(*args, segs=c["segs"], seg_start=c["seg_start"], flags=flags)
-    launches = lib.last_launches()
+    launches, plan = lib.last_launches(), lib.last_split_plan()
     torch.cuda.synchronize()
     assert lib.check() == 0
-    return ref.float().cpu().numpy(), got.float().cpu().numpy(), launches
+    return ref.float().cpu().numpy(), got.float().cpu().numpy(), launches, ref_plan, plan
+
+
+def check_against_oracle(c, got, dtype):
+    o = c["oracle"]
+    want = pa.paged_attention(o["q"], o["kp"], o["vp"], o["table"], o["qsl"], o["seq"], o["q"].shape[2] ** -0.5, 16,
+                              o["segments"])
+    assert np.isfinite(got).all()
+    err = np.abs(got.astype(np.float64) - want)
+    tol_max, tol_mean = TOL[dtype]
+    assert err.max() <= tol_max and err.mean() <= tol_mean, (err.max(), err.mean())
 
 
 CASES = [
@@ -64,22 +86,20 @@ CASES = [
     (1, torch.bfloat16, 8, 2, 128, (300, 212), (900, 700), ([(700, 800)], []), 4),
     (2, torch.bfloat16, 4, 4, 64, (130, 17), (500, 17), ([], [(0, 9)]), 3),
     (3, torch.float32, 4, 2, 64, (40, 33), (120, 90), ([(90, 100)], []), 2),
+    (6, torch.float16, 6, 3, 128, (64, 200), (64, 1000), ([(0, 64)], [(800, 1000)]), 16),
 ]
 
 
-def test_noalloc_matches_workspace_call_on_consecutive_calls(lib):
+def test_noalloc_matches_oracle_and_workspace_call_on_consecutive_calls(lib):
     # Two passes over the cases: every call after the first finds the previous call's data in the scratch.
     for _ in range(2):
         for seed, dtype, hq, hkv, d, sq, kv, spans, splits in CASES:
             c = make_case(seed, dtype, hq, hkv, d, sq, kv, spans)
-            ref, got, launches = run_both(lib, c, lib.PKV_SPLITS(splits))
+            ref, got, launches, ref_plan, plan = run_both(lib, c, lib.PKV_SPLITS(splits))
             assert launches == 2  # split attention + combine: the scratch is in use
-            assert np.isfinite(got).all()
-            err = np.abs(got - ref)
-            if dtype == torch.float32:
-                assert err.max() <= 1e-4
-            else:
-                assert err.max() <= 2e-2 and err.mean() <= 2e-3
+            assert plan == ref_plan and plan[0] == splits, (plan, ref_plan)
+            assert np.array_equal(got, ref)  # same kernels, same plan: the same bits
+            check_against_oracle(c, got, dtype)
 
 
 PLANNED = [
@@ -94,11 +114,21 @@ def test_noalloc_planned_splits(lib):
     for _ in range(2):
         for seed, dtype, hq, hkv, d, sq, kv, spans in PLANNED:
             c = make_case(seed, dtype, hq, hkv, d, sq, kv, spans)
-            ref, got, launches = run_both(lib, c, 0)
-            splits, whole = lib.last_split_plan()
+            ref, got, launches, ref_plan, plan = run_both(lib, c, 0)
+            splits, whole = plan
             assert splits > 1 and whole == 0 and launches == 2, (splits, whole, launches)
-            err = np.abs(got - ref)
-            assert err.max() <= 2e-2 and err.mean() <= 2e-3
+            assert plan == ref_plan, (plan, ref_plan)
+            assert np.array_equal(got, ref)
+            check_against_oracle(c, got, dtype)
+
+
+def test_noalloc_clamps_forced_splits_like_the_workspace_call(lib):
+    # PKV_SPLITS(20) asks for more than the 16 splits either call runs: both take it as 16.
+    c = make_case(7, torch.bfloat16, 4, 2, 64, (100,), (3000,), ([(2900, 3000)],))
+    ref, got, launches, ref_plan, plan = run_both(lib, c, lib.PKV_SPLITS(20))
+    assert plan[0] == 16 and ref_plan[0] == 16 and launches == 2, (plan, ref_plan)
+    assert np.array_equal(got, ref)
+    check_against_oracle(c, got, torch.bfloat16)
 
 
 def test_noalloc_refuses_splits_beyond_its_scratch(lib):
