@@ -50,6 +50,9 @@
 //              P.V of the previous tile is always complete by the time a score
 //              tile is ready (the score MMA was issued after it), so the rescale
 //              never waits.
+// A row's ragged last tile of at most 64 queries (1560 = 6 x 256 + 24) runs alone in its CTA with
+// M = 64 MMAs: half the tensor work (and energy) of M = 128 for the same rows; its accumulator rows
+// sit in lanes 0-15 of each 32-lane TMEM quarter, so half of each softmax warp carries no row.
 // Registers: the producer/MMA warpgroup (warps 0-3) gives up
 // registers to the two softmax warpgroups (setmaxnreg 104 / 200; the launch
 // provides 168 per thread and the host refuses to launch a build with another
@@ -281,7 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool is_softmax = warp >= 4;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
-  const int i = i0 + grp * BM + row;  // local query index of this thread's row
+  // A lone tile of at most 64 rows (a row's ragged last tile) runs M = 64 MMAs, half the tensor work
+  // of M = 128 for the same rows: their accumulator rows sit in lanes 0-15 of each 32-lane TMEM
+  // quarter (row 16q + l at lane 32q + l), so thread (quarter q, lane l < 16) owns row 16q + l and
+  // lanes 16-31 carry no row.
+  const bool m64 = n_q == 1 && Sq - i0 <= 64;
+  const bool row_lane = !m64 || lane < 16;
+  const int i = row_lane ? i0 + grp * BM + (m64 ? quarter * 16 + lane : row) : Sq;  // local query index (Sq: none)
   int lim = 0;
   if (is_softmax && i < Sq) {
     bool uncovered = false;
@@ -352,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = t_end > t_begin ? t_end - t_begin : 0;
 
   constexpr uint32_t O_COL[2] = {256, 256 + D};
-  constexpr uint32_t IDESC_QK = ptx::idesc_f16(BM, BN, BF16 ? 1 : 0, 0);
-  constexpr uint32_t IDESC_PV = ptx::idesc_f16(BM, D, BF16 ? 1 : 0, 1);
+  const uint32_t IDESC_QK = ptx::idesc_f16(m64 ? 64 : BM, BN, BF16 ? 1 : 0, 0);
+  const uint32_t IDESC_PV = ptx::idesc_f16(m64 ? 64 : BM, D, BF16 ? 1 : 0, 1);
 
   if (warp < 4) {
   ptx::regs_dec<kRegsLow>();

@@ -27,6 +27,9 @@ def main() -> None:
     ap.add_argument("--fused", action="store_true", help="paged_kv_write_attn instead of the two calls")
     ap.add_argument("--packed", default=None, help="run this packed batch's attention call instead (configs.PACKED)")
     ap.add_argument("--gather", action="store_true", help="also stage each layer's window (paged_kv_gather)")
+    ap.add_argument("--pool-blocks", type=int, default=None,
+                    help="blocks per layer pool (default: the workload's); a smaller pool keeps a capture's device "
+                         "memory small without changing the blocks the call reads or writes")
     args = ap.parse_args()
     if args.packed:
         from . import packed
@@ -41,6 +44,10 @@ def main() -> None:
         print(f"profile_case: {args.packed}, {args.steps} attention call(s): ok")
         return
     w = configs.ALL[args.workload]
+    if args.pool_blocks:
+        import dataclasses
+
+        w = dataclasses.replace(w, pool_blocks=args.pool_blocks)
     case = workload.build_case(w, device="cuda", layers=args.layers, data_device="cuda")
     st = case.make_staging() if args.gather else None
     for _ in range(args.steps):
