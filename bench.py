@@ -859,19 +859,23 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     e2e_step()
     torch.cuda.synchronize()
     # One step's uploads alone, without compute: the host->device bandwidth this machine gives, so that an
-    # upload-bound step shows as such beside the overlapped one.
-    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(up):
-        u0.record(up)
-        for hd, dd in zip(meta_host, meta_sets[0]):
-            dd.copy_(hd, non_blocking=True)
-        for l in range(layers):
-            io_sets[0][0][l].copy_(host_q[l], non_blocking=True)
-            io_sets[0][1][l].copy_(host_k[l], non_blocking=True)
-            io_sets[0][2][l].copy_(host_v[l], non_blocking=True)
-        u1.record(up)
-    torch.cuda.synchronize()
-    upload_ms = u0.elapsed_time(u1)
+    # upload-bound step shows as such beside the overlapped one.  Taken right before and right after the
+    # timed steps: the link's speed was seen to change over time with no GPU work of this process running.
+    def uploads_alone_ms() -> float:
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(up):
+            u0.record(up)
+            for hd, dd in zip(meta_host, meta_sets[0]):
+                dd.copy_(hd, non_blocking=True)
+            for l in range(layers):
+                io_sets[0][0][l].copy_(host_q[l], non_blocking=True)
+                io_sets[0][1][l].copy_(host_k[l], non_blocking=True)
+                io_sets[0][2][l].copy_(host_v[l], non_blocking=True)
+            u1.record(up)
+        torch.cuda.synchronize()
+        return u0.elapsed_time(u1)
+
+    upload_ms = uploads_alone_ms()
     steps = max(1, min(args.steps, 5))
     barrier(world)
     torch.cuda.synchronize()
@@ -884,6 +888,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
+    upload_ms_after = uploads_alone_ms()
     # The case's tensors again those it started with (the second set and its events go with this function).
     case.q, case.k_new, case.v_new, case.out = io_sets[0]
     for name, t in zip(names, meta_sets[0]):
@@ -894,6 +899,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
             "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
+            "h2d_gbs_alone_after": h2d / (upload_ms_after * 1e-3) / 1e9,
             "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers)),
             "compute_ms_in_last_step": sum(cp_t[l][0].elapsed_time(cp_t[l][1]) for l in range(layers)),
             "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
