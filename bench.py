@@ -413,9 +413,12 @@ def run_ours(args, world, rank, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1), shapes of 832x480 frames)",
         "config": workload_config(w, world),
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 dense (burst)",
+        # The attention calls are timed inside the 40-layer step (about 53 ms of back-to-back launches at the
+        # power cap), so the denominator is the sustained dense bf16 figure; the burst fraction is given beside it.
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops_sustained"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 dense, sustained (the kernel is timed inside the step)",
+                     "frac_of_burst": attn_tflops / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"],
                      "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
                      "kernel": "paged attention (fused with the layer's KV write)" if fused else "paged attention",
                      "ms_per_launch": attn_avg,
@@ -719,6 +722,12 @@ def measure_workload(name: str, stream, peaks: dict, reps: int = 20) -> dict:
     launches = _lib.last_launches()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
     with ClockSampler(torch.cuda.current_device()) as clk:
+        # The same work for about 0.6 s first, so that the 200 ms clock samples land while it runs.
+        t_end = time.perf_counter() + 0.6
+        while time.perf_counter() < t_end:
+            flush.zero_()
+            case.write_attend(0, stream=stream)
+            torch.cuda.synchronize()
         for e0, e1 in ev:
             flush.zero_()
             e0.record(stream)
