@@ -634,7 +634,7 @@ def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
     return res
 
 
-OTHER_WORKLOADS = ("tiny-f32", "one-frame-bf16", "gqa-action-bf16", "mixed-mask-bf16")
+OTHER_WORKLOADS = ("tiny-f32", "one-frame-bf16", "one-frame-partial-bf16", "gqa-action-bf16", "mixed-mask-bf16")
 
 
 def _l2_bytes() -> int:

@@ -19,6 +19,8 @@
 // waits on each store's shared-memory read: 35-55 % with one CTA per SM, 78-85 %
 // with four).
 
+#include <atomic>
+
 #include "kv_copy.cuh"
 
 namespace {
@@ -63,16 +65,20 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const uint4* __restr
   }
 }
 
-// Resident CTAs per SM of one instantiation, per device (queried once).
+// Resident CTAs per SM of one instantiation, per device (queried once; racing first calls from
+// several host threads only store the same value).
 template <typename I>
 int resident_ctas() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_write_kernel<I>, kThreads, 0) != cudaSuccess || n <= 0) n = 4;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
