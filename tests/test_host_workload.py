@@ -47,3 +47,27 @@ def test_metadata_matches_oracle(w):
     for b in range(w.batch):
         n = -(-int(meta.seq_lens[b]) // w.block_size)
         assert 0 not in set(meta.table[b, :n].tolist())
+
+
+@pytest.mark.parametrize("w", list(configs.ALL.values()), ids=lambda w: w.name)
+def test_bench_flop_count_matches_oracle(w):
+    # The bench's algorithmic FLOPs (4 * D * Hq * visible pairs, from the library's segments) equal the
+    # oracle's count over its own metadata: the roofline's numerator does not rest on the bench's arithmetic.
+    import os
+    import sys
+
+    from paged_kv_cache_181_gb300 import build
+
+    if not os.path.exists(build.LIB):
+        build.build()
+    from oracle import pagedattn as pa
+    from paged_kv_cache_181_gb300 import workload
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    rb, ab = synth.allocation(w)
+    meta = workload.build_metadata(w, rb, ab)
+    oc = cases.oracle_metadata(w)
+    want = pa.attention_flops(oc.qsl, oc.seq_lens, oc.segments, w.num_heads, w.head_dim)
+    assert 4 * w.head_dim * w.num_heads * bench.visible_pairs(meta) == want
