@@ -8,16 +8,14 @@
 // lane loading its kU vectors before storing any, and the warps walk the flat
 // list of (row, chunk) pairs with a grid stride, so every warp of a full wave
 // has work even when the rows are few and wide (the long-window workload has
-// 6240 rows of 10 KB for 152 x 48 warps).  Grid: one wave of resident CTAs.
-// Measured against other designs on the workloads' shapes, in bursts of
-// launches on distinct buffers (per launch, % of the measured copy bandwidth):
-//   rows of 6 KB (201 MB): 34.5 us = 86 %; rows of 10 KB (128 MB): 23.0 us =
-//   82 %; rows of 2 KB (52 MB): 12.4 us = 61 %; rows of 3 KB (38 MB): 10.3 us
-//   = 55 % (the small launches pay a fixed ~4-5 us of ramp-up and drain).
+// 6240 rows of 10 KB for 152 x 64 warps).  Grid: one wave of resident CTAs.
+// Measured per launch in bursts on distinct, cold buffers (% of the measured
+// copy bandwidth): rows of 10 KB (128 MB) 22.4 us = 84 %; rows of 6 KB
+// (201 MB) 35.8 us = 83 %; rows of 2 KB (52 MB) 10.3 us = 74 %; rows of 3 KB
+// (38 MB) 8.2 us = 69 % (a launch pays a fixed few us of ramp-up and drain).
 // One warp per whole row, all of it in registers, measured the same; TMA bulk
 // copies staged through shared memory were slower (one issuing thread per CTA
-// waits on each store's shared-memory read: 35-55 % with one CTA per SM, 78-85 %
-// with four).
+// waits on each store's shared-memory read).
 
 #include <atomic>
 
