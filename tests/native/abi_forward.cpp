@@ -1,6 +1,8 @@
 // One layer's forward through the C ABI alone -- no Python, no torch types: host metadata from the
 // library's own functions, device memory from cudaMalloc, the fused write + attention call, the
-// device error word read back with pkv_check.
+// device error word read back with pkv_check.  Then the same layer's attention again through
+// paged_attn_varlen_noalloc (the pools now hold the chunk), as a caller without an allocator would
+// run it: no workspace, the library's fixed scratch.
 //
 // usage: abi_forward <dir>
 //   <dir>/params.txt   B Hq Hkv D pool_blocks chunk sink window action_len history query_tokens n_spans
@@ -8,7 +10,7 @@
 //   <dir>/row_blocks.i32      B x ceil((history + query_tokens) / 16) physical blocks (video, per row)
 //   <dir>/action_blocks.i32   B x ceil(action_len / 16) scratch blocks (per row), absent when action_len = 0
 //   <dir>/q.bf16, k_hist.bf16, v_hist.bf16, k_cur.bf16, v_cur.bf16   raw bf16 (see the sizes below)
-// writes <dir>/out.bf16: [B * (query_tokens + action_len), Hq, D]
+// writes <dir>/out.bf16 (fused call) and <dir>/out_noalloc.bf16: [B * (query_tokens + action_len), Hq, D]
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -151,7 +153,22 @@ int main(int argc, char** argv) {
   CHECK_CUDA(cudaMemcpy(h_out.data(), out, h_out.size() * sizeof(uint16_t), cudaMemcpyDeviceToHost));
   std::ofstream of(dir + "/out.bf16", std::ios::binary);
   of.write(reinterpret_cast<const char*>(h_out.data()), (std::streamsize)(h_out.size() * sizeof(uint16_t)));
-  std::printf("abi_forward: %s, %lld tokens x %lld heads, launches %d, device bits 0x%x\n", pkv_version(),
-              (long long)Tq, (long long)Hq, pkv_last_launches(), bits);
+  const int launches = pkv_last_launches();
+
+  // The attention alone, allocation-free: split partials (if any) in the library's fixed scratch.
+  CHECK_CUDA(cudaMemset(out, 0, h_out.size() * sizeof(uint16_t)));
+  CHECK_PKV(paged_attn_varlen_noalloc(d_q, Tq, (int)Hq, kp, vp, pool_blocks, bs, (int)Hkv, (int)D, PKV_BF16, d_table,
+                                      (int)B, (int)W, d_qsl, d_seq, (int)q_len, (int)(W * bs),
+                                      1.0f / std::sqrt((float)D), d_segs, d_seg_start, out, PKV_CHECK_BOUNDS,
+                                      nullptr));
+  const int launches_noalloc = pkv_last_launches();
+  uint32_t bits_noalloc = 0;
+  CHECK_PKV(pkv_check(nullptr, &bits_noalloc));
+  CHECK_CUDA(cudaMemcpy(h_out.data(), out, h_out.size() * sizeof(uint16_t), cudaMemcpyDeviceToHost));
+  std::ofstream of2(dir + "/out_noalloc.bf16", std::ios::binary);
+  of2.write(reinterpret_cast<const char*>(h_out.data()), (std::streamsize)(h_out.size() * sizeof(uint16_t)));
+  std::printf("abi_forward: %s, %lld tokens x %lld heads, launches %d, device bits 0x%x; noalloc launches %d, "
+              "device bits 0x%x\n",
+              pkv_version(), (long long)Tq, (long long)Hq, launches, bits, launches_noalloc, bits_noalloc);
   return 0;
 }

@@ -1,9 +1,10 @@
 """The C ABI driven from C++ alone (tests/native/abi_forward.cpp): no Python binding, no torch types.
 
 The program computes the host metadata with the library's own functions, allocates device memory with
-cudaMalloc, writes the history with paged_kv_write and runs the layer with paged_kv_write_attn.  The CPU
-test builds it against include/pagedkv.h and libpagedkv.so; the GPU test feeds it seeded inputs and
-compares its output with the oracle.
+cudaMalloc, writes the history with paged_kv_write and runs the layer with paged_kv_write_attn, then the
+same attention through paged_attn_varlen_noalloc (no workspace).  The CPU test builds it against
+include/pagedkv.h and libpagedkv.so; the GPU test feeds it seeded inputs and compares both outputs with
+the oracle, and with each other bit for bit.
 """
 
 import dataclasses
@@ -64,11 +65,19 @@ def test_native_forward_matches_oracle(tmp_path):
         t.contiguous().view(torch.int16).numpy().tofile(tmp_path / f"{name}.bf16")
     res = subprocess.run([exe, str(tmp_path)], capture_output=True, text=True, timeout=120)
     assert res.returncode == 0, res.stdout + res.stderr
-    assert "device bits 0x0" in res.stdout
+    assert "device bits 0x0" in res.stdout and "noalloc launches" in res.stdout
+    assert res.stdout.rstrip().endswith("device bits 0x0"), res.stdout
     tq = w.batch * w.q_len
-    raw = np.fromfile(tmp_path / "out.bf16", dtype=np.int16).reshape(tq, w.num_heads, w.head_dim)
-    got = torch.from_numpy(raw).view(torch.bfloat16).float().numpy()
     oc = cases.oracle_metadata(w)
     cases.oracle_pools(w, d, oc)
-    max_abs, mean_abs = cases.compare(got, cases.expected(w, oc), "bf16")
-    assert max_abs <= cases.TOL["bf16"][0] and mean_abs <= cases.TOL["bf16"][1], (max_abs, mean_abs)
+    want = cases.expected(w, oc)
+    raws = []
+    for name in ("out.bf16", "out_noalloc.bf16"):
+        raw = np.fromfile(tmp_path / name, dtype=np.int16).reshape(tq, w.num_heads, w.head_dim)
+        raws.append(raw)
+        got = torch.from_numpy(raw).view(torch.bfloat16).float().numpy()
+        max_abs, mean_abs = cases.compare(got, want, "bf16")
+        assert max_abs <= cases.TOL["bf16"][0] and mean_abs <= cases.TOL["bf16"][1], (name, max_abs, mean_abs)
+    # Same kernels, same keys (the fused call reads the chunk from k/v, the second call from the pools it
+    # wrote), same split plan: the same bits.
+    assert np.array_equal(raws[0], raws[1])
