@@ -345,9 +345,9 @@ def run_ours(args, world, rank, local):
     # KV write: a burst of one write per layer (a single ~20 us launch is too short to time alone), each
     # write into its own cold layer pool, replayed from a CUDA graph.
     write_avg = graph_burst_ms([lambda l=l: case.write(l) for l in range(layers)], stream)
-    # The attention launch as the step runs it: the fused write + attention, or (two-call form)
-    # the attention call after its layer's write.
-    for _ in range(max(1, min(args.steps, 3))):
+    # The launches of one step as it runs them: the fused write + attention, or (two-call form) the
+    # attention call after its layer's write.
+    for _ in range(1):
         for l in range(layers):
             if not fused:
                 ev_w[l][0].record(stream)
@@ -367,17 +367,30 @@ def run_ours(args, world, rank, local):
         attn_launches = launch_log[-layers:]
         attn_ms += [ev_a[l][0].elapsed_time(ev_a[l][1]) for l in range(layers)]
 
-    # Timed region: K whole steps.
+    # Timed region: K whole steps.  Each layer's attention call is bracketed by events inside the timed
+    # steps themselves, so the per-call duration behind the roofline is taken at the clock the step runs at
+    # (steps started from idle run faster until the power cap settles).
+    ev_t = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+            for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         start.record(stream)
-        for _ in range(args.steps):
-            step()
+        for k in range(args.steps):
+            for l in range(layers):
+                if not fused:
+                    case.write(l, stream=stream)
+                ev_t[k][l][0].record(stream)
+                if fused:
+                    case.write_attend(l, stream=stream)
+                else:
+                    case.attend(l, stream=stream)
+                ev_t[k][l][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
+    attn_ms = [e0.elapsed_time(e1) for row in ev_t for e0, e1 in row]
     ms = max_over_ranks(start.elapsed_time(end), world)
     ms_step = ms / args.steps
     total_flops = flops_per_layer * layers * world
@@ -582,7 +595,7 @@ def measure_packed(stream, peaks: dict, reps: int = 10) -> dict:
     return res
 
 
-def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
+def measure_kv_layout(case, stream, step_call_ms: float, row_bytes: int) -> dict:
     """Per layer: the block gather of the visible window into staging buffers, the same attention on the
     staged (contiguous) K/V, and the re-gather of the current chunk's blocks only (history kept staged)."""
     import torch
@@ -608,22 +621,30 @@ def measure_kv_layout(case, stream, paged_ms: float, row_bytes: int) -> dict:
 
     gather_ms = burst(lambda l: case.stage(l, st, stream=stream))
     regather_ms = burst(lambda l: case.stage(l, st, reuse_history=True, stream=stream))
-    # Attention on staged K/V: events around each launch, every layer staged just before.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
-    contig_ms = []
+    # The same attention call (paged_attn_varlen) on the pools and on staged K/V, alternating layer by layer so
+    # both run at the same clock: events around each launch, every layer staged just before.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)]
+    contig_ms, paged_only_ms = [], []
     for _ in range(2):
         for l in range(layers):
             case.stage(l, st, stream=stream)
             ev[l][0].record(stream)
-            case.attend_contiguous(l, st, stream=stream)
+            case.attend(l, stream=stream)
             ev[l][1].record(stream)
+            ev[l][2].record(stream)
+            case.attend_contiguous(l, st, stream=stream)
+            ev[l][3].record(stream)
         torch.cuda.synchronize()
-        contig_ms += [ev[l][0].elapsed_time(ev[l][1]) for l in range(layers)]
+        paged_only_ms += [ev[l][0].elapsed_time(ev[l][1]) for l in range(layers)]
+        contig_ms += [ev[l][2].elapsed_time(ev[l][3]) for l in range(layers)]
     contig = statistics.mean(contig_ms)
+    paged_ms = statistics.mean(paged_only_ms)
     staged_rows = case.w.batch * st.used_blocks * case.w.block_size
     chunk_rows = case.w.batch * (st.used_blocks - st.first_block) * case.w.block_size
     res = {
         "paged_attn_ms": paged_ms, "contiguous_attn_ms": contig, "paged_over_contiguous": paged_ms / contig,
+        "api": "paged_attn_varlen on the pools and on the staged window, alternating per layer",
+        "fused_step_call_ms": step_call_ms,
         "gather_ms": gather_ms, "gather_gbs": staged_rows * row_bytes * 4 / (gather_ms * 1e-3) / 1e9,
         "regather_chunk_ms": regather_ms, "regather_blocks_per_row": st.used_blocks - st.first_block,
         "gather_then_attend_ms": gather_ms + contig, "regather_then_attend_ms": regather_ms + contig,
