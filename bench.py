@@ -439,6 +439,9 @@ def run_ours(args, world, rank, local):
         "kv_write": {"bound": "hbm", "achieved": write_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": write_gbs / peaks["hbm_gbs"], "ms_per_launch": write_avg,
                      "algorithmic_bytes_per_launch": write_bytes_per_layer,
+                     "traffic": read_traffic(w.name, "kv_write_long_window.md", WRITE_KERNEL_REV),
+                     "traffic_note": "DRAM read + write during one launch (ncu); the rest of the pool rows is "
+                                     "written back from L2 after it",
                      "kernel": "paged_kv_write (standalone launch; inside the fused call it overlaps the attention)"},
         "gpu_launches": args.steps * launches_per_step,
         "step_api": "paged_kv_write_attn per layer (write fused into the attention launch)" if fused
@@ -774,15 +777,18 @@ def measure_workload(name: str, stream, peaks: dict, reps: int = 20) -> dict:
     return res
 
 
-def read_traffic(workload_name: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken of this kernel revision."""
+WRITE_KERNEL_REV = "w-v2"
+
+
+def read_traffic(workload_name: str, summary: str = "attn_tc_long_window.md", rev: str | None = None):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken of this kernel revision."""
     import re
 
-    path = os.path.join(ROOT, "profiles", "attn_tc_long_window.md")
+    path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
     m = re.search(r"traffic: workload=(\S+) rev=(\S+) bytes_per_launch=(\d+)", open(path).read())
-    if not m or m.group(1) != workload_name or m.group(2) != KERNEL_REV:
+    if not m or m.group(1) != workload_name or m.group(2) != (KERNEL_REV if rev is None else rev):
         return None
     return int(m.group(3))
 
