@@ -1,49 +1,109 @@
 // CUDA-core paged attention (fp32 arithmetic throughout) and the split-KV combine.
 //
 // This is the kernel for fp32 inputs, where tensor-core tf32 would not meet a
-// 1e-4 tolerance, and for shapes the tcgen05 kernel does not take.  It computes
+// 1e-4 tolerance, and for calls that ask for it (PKV_FORCE_SIMT).  It computes
 // what _reference_paged_attention (paged_attention.py) computes -- gather each
 // key through the block table, softmax(scale * q.k) over the visible keys,
 // weighted sum of values -- with the piecewise causal/full mask of
 // piecewise_attn.py expressed as a per-query key limit, and an online
 // (running max / running sum) softmax so the key range can be streamed.
 //
-// CTA = 16 queries of one (row, head) and one key-range split; 4 warps, each
-// owning 4 queries; keys staged 32 at a time in shared memory as fp32.
+// CTA = 64 queries of one (row, head) and one key-range split; 256 threads as a
+// 16 x 16 grid (ty, tx).  Per 64-key tile, all in fp32 shared memory:
+//   S = Q K^T  thread (ty, tx) owns rows ty + 16i and keys tx + 16j (i, j < 4):
+//              per 4 dimensions it loads 4 query and 4 key float4s and does 64
+//              FMAs (rows and keys interleaved by 16, so a warp's key loads hit
+//              distinct banks and its query loads are broadcasts);
+//   softmax    each row's 64 scores sit in the 16 threads of one half-warp:
+//              maxima and sums by shuffles; P goes to shared memory transposed;
+//   O += P V   thread (ty, tx) owns rows 4ty..4ty+3 and columns 4tx + 64c:
+//              per key one float4 of P and D/64 float4s of V for 16 D/64 FMAs.
 
 #include <math.h>
+#include <string.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kv_copy.cuh"
 
 namespace {
 
-constexpr int kQT = 16;      // queries per CTA
-constexpr int kKT = 32;      // keys per shared-memory tile
-constexpr int kWarps = 4;
-constexpr int kRowsPerWarp = kQT / kWarps;
+constexpr int kSQ = kSimtItemRows;  // queries per CTA
+constexpr int kSK = kSimtKeyTile;   // keys per tile
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
+
+template <int D>
+struct SimtSmem {
+  static constexpr int LD = D + 4;    // row stride (floats) of Q, K and V: 16-byte rows, staggered banks
+  static constexpr int PL = kSQ + 4;  // row stride of P^T
+  // Q, two K/V buffers (the next tile loads while this one is used), P^T, per-row state.
+  static constexpr size_t floats = (size_t)kSQ * LD + (size_t)4 * kSK * LD + (size_t)kSK * PL + 3 * kSQ;
+  static constexpr size_t bytes = floats * sizeof(float) + (kSQ + 1) * sizeof(int);
+};
+
+// 16-byte asynchronous copy global -> shared; `bytes` 0 zero-fills the destination without a read.
+PKV_DEVINLINE void cp_async16(float* dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+
+// Four consecutive elements as fp32 (16-byte aligned for fp32, 8-byte for 16-bit types).
+template <typename T>
+PKV_DEVINLINE float4 load4(const T* __restrict__ p) {
+  if constexpr (sizeof(T) == 4) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+  } else {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    T t[4];
+    memcpy(t, &u, sizeof(u));
+    return make_float4(pkv_to_f32<T>(t[0]), pkv_to_f32<T>(t[1]), pkv_to_f32<T>(t[2]), pkv_to_f32<T>(t[3]));
+  }
+}
 
 template <typename T>
-PKV_DEVINLINE void load_row_f32(const T* __restrict__ src, float* dst, int D, int lane_in_group, int group_size) {
-  for (int d = lane_in_group; d < D; d += group_size) dst[d] = pkv_to_f32<T>(src[d]);
+PKV_DEVINLINE void store4(T* p, float x0, float x1, float x2, float x3) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(x0, x1, x2, x3);
+  } else {
+    T t[4] = {pkv_from_f32<T>(x0), pkv_from_f32<T>(x1), pkv_from_f32<T>(x2), pkv_from_f32<T>(x3)};
+    uint2 u;
+    memcpy(&u, t, sizeof(u));
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+}
+
+PKV_DEVINLINE float dot4(float4 a, float4 b, float acc) {
+  acc = fmaf(a.x, b.x, acc);
+  acc = fmaf(a.y, b.y, acc);
+  acc = fmaf(a.z, b.z, acc);
+  return fmaf(a.w, b.w, acc);
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
-  __shared__ float q_s[kQT][D];
-  __shared__ float k_s[kKT][D + 1];
-  __shared__ float v_s[kKT][D];
-  __shared__ int lim_s[kQT];
-  __shared__ int kv_hi_s;
+__global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) {
+  using SM = SimtSmem<D>;
+  constexpr int LD = SM::LD, PL = SM::PL, NC = D / 64;
+  extern __shared__ __align__(16) float sm[];
+  float* q_s = sm;                          // [kSQ][LD]
+  float* kv_buf = q_s + kSQ * LD;           // two buffers of [kSK][LD] keys then [kSK][LD] values
+  float* p_s = kv_buf + 4 * kSK * LD;       // [kSK][PL], P transposed: p_s[key * PL + query]
+  float* alpha_s = p_s + kSK * PL;  // [kSQ] per-tile rescale of each row's O
+  float* l_s = alpha_s + kSQ;       // [kSQ]
+  float* m_s = l_s + kSQ;           // [kSQ]
+  int* lim_s = reinterpret_cast<int*>(m_s + kSQ);  // [kSQ], then the CTA's largest limit
+  int* kv_hi_s = lim_s + kSQ;
 
-  const int tiles_per_row = (a.max_query_len + kQT - 1) / kQT;
+  const int tiles_per_row = (a.max_query_len + kSQ - 1) / kSQ;
   const int b = blockIdx.x / tiles_per_row;
   const int tile = blockIdx.x % tiles_per_row;
   const int h = blockIdx.y;
   const int split = blockIdx.z;
   const int kvh = h / (a.Hq / a.Hkv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ty = tid >> 4, tx = tid & 15;
 
   const int q0 = a.query_start_loc[b];
   const int q1 = a.query_start_loc[b + 1];
@@ -66,155 +126,241 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(PkvAttnArgs a) {
   if (a.k_new) {
     const int64_t cta = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     pkv_scatter((const uint4*)a.k_new, (const uint4*)a.v_new, a.slots, a.Tq, (uint4*)a.k_pool, (uint4*)a.v_pool,
-                a.num_slots, a.Hkv * D * (int)sizeof(T) / 16, a.err, a.check, cta * kWarps + warp,
-                (int64_t)gridDim.x * gridDim.y * gridDim.z * kWarps, lane, &a);
+                a.num_slots, a.Hkv * D * (int)sizeof(T) / 16, a.err, a.check, cta * kSWarps + warp,
+                (int64_t)gridDim.x * gridDim.y * gridDim.z * kSWarps, lane, &a);
   }
-  const int i0 = tile * kQT;
+  const int i0 = tile * kSQ;
   if (i0 >= Sq) return;
 
+  int s_begin = 0, s_end = 0;
+  if (a.segs) {
+    s_begin = a.seg_start[b];
+    s_end = a.seg_start[b + 1];
+  }
+  const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
   // Per-query key limits from the row's segments.
-  if (tid < kQT) {
+  if (tid < kSQ) {
     const int i = i0 + tid;
     int lim = 0;
     if (i < Sq) {
       bool uncovered = false;
-      int s_begin = 0, s_end = 0;
-      if (a.segs) {
-        s_begin = a.seg_start[b];
-        s_end = a.seg_start[b + 1];
-      }
-      const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
       lim = pkv_row_limit(base + i, L, a.segs, s_begin, s_end, &uncovered);
       if (a.check && (uncovered || base < 0 || base + Sq > L)) pkv_raise(a.err, PKV_DEVERR_SEGMENT);
     }
     lim_s[tid] = lim;
   }
-  // Query tile, fp32 in shared memory.
-  for (int e = tid; e < kQT * D; e += blockDim.x) {
-    const int r = e / D, d = e % D;
+  // Query tile, fp32 in shared memory (rows past the row's queries are zero).
+  for (int e = tid; e < kSQ * (D / 4); e += kSThreads) {
+    const int r = e / (D / 4), c = (e % (D / 4)) * 4;
     const int i = i0 + r;
-    q_s[r][d] = i < Sq ? pkv_to_f32<T>(((const T*)a.q)[((int64_t)(q0 + i) * a.Hq + h) * D + d]) : 0.f;
+    const float4 x = i < Sq ? load4<T>((const T*)a.q + ((int64_t)(q0 + i) * a.Hq + h) * D + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(q_s + r * LD + c) = x;
   }
   __syncthreads();
-  if (tid == 0) {
-    int hi = 0;
-    for (int r = 0; r < kQT; ++r) hi = lim_s[r] > hi ? lim_s[r] : hi;
-    kv_hi_s = hi;
+  if (warp == 0) {
+    int hi = lim_s[lane] > lim_s[lane + 32] ? lim_s[lane] : lim_s[lane + 32];
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) *kv_hi_s = hi;
   }
   __syncthreads();
-  const int kv_hi = kv_hi_s;
+  const int kv_hi = *kv_hi_s;
 
   // This split's range of key tiles.
-  const int n_tiles = (kv_hi + kKT - 1) / kKT;
+  const int n_tiles = (kv_hi + kSK - 1) / kSK;
   const int per = (n_tiles + a.num_splits - 1) / a.num_splits;
   const int t_begin = split * per;
   const int t_end = min(n_tiles, t_begin + per);
 
-  constexpr int kDL = D / 32;  // accumulator columns per lane
-  float acc[kRowsPerWarp][kDL];
-  float m[kRowsPerWarp], l[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
-#pragma unroll
-    for (int c = 0; c < kDL; ++c) acc[r][c] = 0.f;
-  }
-
+  // Keys at the queries' own positions [cb, ce): read from the new tokens in a fused call.
+  const int cb = a.k_new ? base : 0, ce = a.k_new ? base + Sq : 0;
   const T* kpool = (const T*)a.k_pool;
   const T* vpool = (const T*)a.v_pool;
-  // Keys at the queries' own positions [cb, ce): read from the new tokens in a fused call.
-  int cb = 0, ce = 0;
-  if (a.k_new) {
-    int s_begin = 0, s_end = 0;
-    if (a.segs) {
-      s_begin = a.seg_start[b];
-      s_end = a.seg_start[b + 1];
-    }
-    cb = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
-    ce = cb + Sq;
+
+  int lim_r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lim_r[i] = lim_s[ty + 16 * i];
+  float m[4], l[4];  // softmax state of rows ty + 16i (the same in all 16 threads of the half-warp)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
   }
-  for (int kt = t_begin; kt < t_end; ++kt) {
-    const int j0 = kt * kKT;
-    __syncthreads();
-    // Gather 32 keys/values through the block table; 4 threads per key row.
-    {
-      const int jj = tid >> 2, part = tid & 3;
+  float acc[4][4 * NC];  // O rows 4ty + i, columns 4tx + 64c + e
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int c = 0; c < 4 * NC; ++c) acc[i][c] = 0.f;
+
+  // Gather 64 keys and values of tile kt through the block table into buffer `buf` (fp32); past
+  // kv_hi: zeros.  fp32 sources go by asynchronous 16-byte copies (the next tile lands while this one
+  // is used); 16-bit ones are loaded and converted.
+  auto gather = [&](int kt, int buf) {
+    float* kd = kv_buf + buf * 2 * kSK * LD;
+    float* vd = kd + kSK * LD;
+    const int j0 = kt * kSK;
+    for (int e = tid; e < kSK * (D / 4); e += kSThreads) {
+      const int jj = e / (D / 4), c = (e % (D / 4)) * 4;
       const int j = j0 + jj;
+      const T* ks = nullptr;
+      const T* vs = nullptr;
       if (j < kv_hi && j >= cb && j < ce) {
-        const int64_t tok = (int64_t)q0 + (j - cb);
-        load_row_f32<T>((const T*)a.k_new + (tok * a.Hkv + kvh) * D, k_s[jj], D, part, 4);
-        load_row_f32<T>((const T*)a.v_new + (tok * a.Hkv + kvh) * D, v_s[jj], D, part, 4);
+        const int64_t off = (((int64_t)q0 + (j - cb)) * a.Hkv + kvh) * D + c;
+        ks = (const T*)a.k_new + off;
+        vs = (const T*)a.v_new + off;
       } else if (j < kv_hi) {
         int blk = a.block_table[(int64_t)b * a.W + (j >> 4)];
         if (a.check && (blk < 0 || blk >= a.num_blocks)) {
           pkv_raise(a.err, PKV_DEVERR_BLOCK);
-          blk = 0;
+          blk = -1;
         }
-        const int64_t row = (int64_t)blk * 16 + (j & 15);
-        const T* ksrc = kpool + (row * a.Hkv + kvh) * D;
-        const T* vsrc = vpool + (row * a.Hkv + kvh) * D;
-        load_row_f32<T>(ksrc, k_s[jj], D, part, 4);
-        load_row_f32<T>(vsrc, v_s[jj], D, part, 4);
+        if (blk >= 0) {
+          const int64_t off = (((int64_t)blk * 16 + (j & 15)) * a.Hkv + kvh) * D + c;
+          ks = kpool + off;
+          vs = vpool + off;
+        }
+      }
+      if constexpr (sizeof(T) == 4) {
+        cp_async16(kd + jj * LD + c, ks ? (const void*)ks : a.k_pool, ks ? 16 : 0);
+        cp_async16(vd + jj * LD + c, vs ? (const void*)vs : a.v_pool, vs ? 16 : 0);
       } else {
-        for (int d = part; d < D; d += 4) {
-          k_s[jj][d] = 0.f;
-          v_s[jj][d] = 0.f;
-        }
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(kd + jj * LD + c) = ks ? load4<T>(ks) : z;
+        *reinterpret_cast<float4*>(vd + jj * LD + c) = vs ? load4<T>(vs) : z;
       }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  if (t_begin < t_end) gather(t_begin, 0);
+  for (int kt = t_begin; kt < t_end; ++kt) {
+    const int j0 = kt * kSK;
+    const int buf = (kt - t_begin) & 1;
+    const float* k_s = kv_buf + buf * 2 * kSK * LD;
+    const float* v_s = k_s + kSK * LD;
+    __syncthreads();  // the previous tile's buffer and P are no longer read
+    if (kt + 1 < t_end) {
+      gather(kt + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's copies have landed
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     __syncthreads();
+
+    // S = Q K^T for rows ty + 16i, keys tx + 16j.
+    float s[4][4];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int qr = warp * kRowsPerWarp + r;
-      const int lim = lim_s[qr];
-      const int j = j0 + lane;
-      float s = -INFINITY;
-      if (j < lim) {
-        float dot = 0.f;
-#pragma unroll 8
-        for (int d = 0; d < D; ++d) dot = fmaf(q_s[qr][d], k_s[lane][d], dot);
-        s = dot * a.scale;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; d += 4) {
+      float4 qv[4], kv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kv[j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[i][j] = dot4(qv[i], kv[j], s[i][j]);
+    }
+    // Online softmax per row: the row's 64 scores live in this half-warp (lanes with the same ty).
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s[i][j] = j0 + tx + 16 * j < lim_r[i] ? s[i][j] * a.scale : -INFINITY;
+        tmax = fmaxf(tmax, s[i][j]);
       }
-      float tmax = s;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-      const float m_new = fmaxf(m[r], tmax);
-      if (m_new == -INFINITY) continue;  // nothing visible yet for this query
-      const float p = j < lim ? expf(s - m_new) : 0.f;
-      const float alpha = expf(m[r] - m_new);  // exp(-inf) = 0 on the first visible tile
-      float psum = p;
+      for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      const float m_new = fmaxf(m[i], tmax);
+      float alpha = 1.f, psum = 0.f;
+      if (m_new != -INFINITY) {  // else: nothing visible yet for this query; P = 0, O unchanged
+        alpha = expf(m[i] - m_new);  // exp(-inf) = 0 on the first visible tile
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-      l[r] = l[r] * alpha + psum;
-      m[r] = m_new;
+        for (int j = 0; j < 4; ++j) {
+          const float p = s[i][j] == -INFINITY ? 0.f : expf(s[i][j] - m_new);
+          s[i][j] = p;
+          psum += p;
+        }
+      } else {
 #pragma unroll
-      for (int c = 0; c < kDL; ++c) acc[r][c] *= alpha;
-      for (int jj = 0; jj < kKT; ++jj) {
-        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+      }
 #pragma unroll
-        for (int c = 0; c < kDL; ++c) acc[r][c] = fmaf(pj, v_s[jj][lane + 32 * c], acc[r][c]);
+      for (int o = 8; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+      if (m_new != -INFINITY) {
+        l[i] = l[i] * alpha + psum;
+        m[i] = m_new;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p_s[(tx + 16 * j) * PL + ty + 16 * i] = s[i][j];
+      if (tx == 0) alpha_s[ty + 16 * i] = alpha;
+    }
+    __syncthreads();
+
+    // O += P V for rows 4ty + i, columns 4tx + 64c.
+    {
+      const float4 al = *reinterpret_cast<const float4*>(alpha_s + 4 * ty);
+      const float alr[4] = {al.x, al.y, al.z, al.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 4 * NC; ++c) acc[i][c] *= alr[i];
+#pragma unroll 4
+      for (int k = 0; k < kSK; ++k) {
+        const float4 pv = *reinterpret_cast<const float4*>(p_s + k * PL + 4 * ty);
+        const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float4 vv = *reinterpret_cast<const float4*>(v_s + k * LD + 4 * tx + 64 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[i][4 * c + 0] = fmaf(pr[i], vv.x, acc[i][4 * c + 0]);
+            acc[i][4 * c + 1] = fmaf(pr[i], vv.y, acc[i][4 * c + 1]);
+            acc[i][4 * c + 2] = fmaf(pr[i], vv.z, acc[i][4 * c + 2]);
+            acc[i][4 * c + 3] = fmaf(pr[i], vv.w, acc[i][4 * c + 3]);
+          }
+        }
       }
     }
   }
 
-  // Epilogue: normalised output, or partial output + log-sum-exp per split.
+  // Epilogue: each row's softmax state to shared memory, then the normalised output (one split),
+  // or the partial output and its natural-log log-sum-exp (a key-range split).
+  if (tx == 0) {
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int i = i0 + warp * kRowsPerWarp + r;
-    if (i >= Sq) continue;
-    const int64_t tok = q0 + i;
-    const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+    for (int i = 0; i < 4; ++i) {
+      l_s[ty + 16 * i] = l[i];
+      m_s[ty + 16 * i] = m[i];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * ty + i;
+    const int qi = i0 + r;
+    if (qi >= Sq) continue;
+    const int64_t tok = (int64_t)q0 + qi;
+    const float lr = l_s[r];
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
     if (a.num_splits == 1) {
       T* o = (T*)a.out + (tok * a.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < kDL; ++c) o[lane + 32 * c] = pkv_from_f32<T>(acc[r][c] * inv);
+      for (int c = 0; c < NC; ++c)
+        store4<T>(o + 4 * tx + 64 * c, acc[i][4 * c] * inv, acc[i][4 * c + 1] * inv, acc[i][4 * c + 2] * inv,
+                  acc[i][4 * c + 3] * inv);
     } else {
       float* o = a.part_o + (((int64_t)split * a.Tq + tok) * a.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < kDL; ++c) o[lane + 32 * c] = acc[r][c] * inv;
-      if (lane == 0)
-        a.part_lse[((int64_t)split * a.Tq + tok) * a.Hq + h] = l[r] > 0.f ? m[r] + logf(l[r]) : -INFINITY;
+      for (int c = 0; c < NC; ++c)
+        store4<float>(o + 4 * tx + 64 * c, acc[i][4 * c] * inv, acc[i][4 * c + 1] * inv, acc[i][4 * c + 2] * inv,
+                      acc[i][4 * c + 3] * inv);
+      if (tx == 0)
+        a.part_lse[((int64_t)split * a.Tq + tok) * a.Hq + h] = lr > 0.f ? m_s[r] + logf(lr) : -INFINITY;
     }
   }
 }
@@ -332,15 +478,30 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
     combine_row<T, 2>(a, item, lane);
 }
 
+template <typename T, int D>
+int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
+  const size_t smem = SimtSmem<D>::bytes;
+  // Keyed on the context: function attributes belong to the context they were set in.
+  static std::atomic<uint64_t> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool cached = dev >= 0 && dev < 64;
+  const uint64_t ctx = pkv_context_id();
+  if (!cached || ctx == 0 || attr_set[dev].load(std::memory_order_acquire) != ctx) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    if (cached) attr_set[dev].store(ctx, std::memory_order_release);
+  }
+  const int tiles_per_row = (a.max_query_len + kSQ - 1) / kSQ;
+  dim3 grid((unsigned)(a.B * tiles_per_row), (unsigned)a.Hq, (unsigned)a.num_splits);
+  attn_simt_kernel<T, D><<<grid, kSThreads, smem, s>>>(a);
+  return (int)cudaGetLastError();
+}
+
 template <typename T>
 int launch_simt_t(const PkvAttnArgs& a, cudaStream_t s) {
-  const int tiles_per_row = (a.max_query_len + kQT - 1) / kQT;
-  dim3 grid((unsigned)(a.B * tiles_per_row), (unsigned)a.Hq, (unsigned)a.num_splits);
-  if (a.D == 64)
-    attn_simt_kernel<T, 64><<<grid, kWarps * 32, 0, s>>>(a);
-  else
-    attn_simt_kernel<T, 128><<<grid, kWarps * 32, 0, s>>>(a);
-  return (int)cudaGetLastError();
+  return a.D == 64 ? launch_simt_d<T, 64>(a, s) : launch_simt_d<T, 128>(a, s);
 }
 
 }  // namespace

@@ -199,15 +199,15 @@ SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits, boo
 }  // namespace
 
 // Key-range splits the call plans from host-visible sizes.  An item is what one CTA of the
-// unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 16 for the
+// unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 64 for the
 // CUDA-core one.  Only the tensor-core kernel splits a tail behind whole items; the CUDA-core
 // kernel splits all of its items or none (only when they leave SMs idle).
 static SplitPlan planned_splits(int B, int Hq, int max_query_len, int max_seq_len, bool tc, int sms) {
-  const int64_t q_unit = tc ? kTcItemRows : 16;
-  const int64_t k_tile = tc ? 128 : 32;
+  const int64_t q_unit = tc ? kTcItemRows : kSimtItemRows;
+  const int64_t k_tile = tc ? 128 : kSimtKeyTile;
   const int64_t items = (int64_t)B * Hq * ((max_query_len + q_unit - 1) / q_unit);
   const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
-  SplitPlan p = plan_splits(items, tiles, tc ? sms : sms * 8, kMaxSplits, tc);
+  SplitPlan p = plan_splits(items, tiles, tc ? sms : sms * kSimtCtasPerSm, kMaxSplits, tc);
   if (!tc) p.direct = 0;
   return p;
 }

@@ -20,6 +20,12 @@ inline int pkv_dtype_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
 // Most key-range splits per item; larger PKV_SPLITS(n) requests are clamped to it.
 constexpr int kPkvMaxSplits = 16;
 
+// CUDA-core attention kernel: queries per CTA, keys per tile, CTAs resident per SM (its shared memory
+// holds the fp32 Q, K, V and P tiles: one CTA per SM for D = 128).  The split planner counts in these.
+constexpr int kSimtItemRows = 64;
+constexpr int kSimtKeyTile = 64;
+constexpr int kSimtCtasPerSm = 1;
+
 // Process-unique id of the CUDA context current on this thread (0: none, or the driver call is
 // unavailable).  Per-device caches of device addresses and function attributes are keyed on it, so
 // that a new context on the same device (after cudaDeviceReset, or a caller's own context) looks
