@@ -658,7 +658,21 @@ def measure_kv_layout(case, stream, step_call_ms: float, row_bytes: int) -> dict
     return res
 
 
-OTHER_WORKLOADS = ("tiny-f32", "one-frame-bf16", "one-frame-partial-bf16", "gqa-action-bf16", "mixed-mask-bf16")
+OTHER_WORKLOADS = ("tiny-f32", "one-frame-bf16", "one-frame-partial-bf16", "gqa-action-bf16", "mixed-mask-bf16",
+                   "long-window-f32-1L")
+
+
+def fp32_fma_peak_tflops() -> float:
+    """CUDA-core fp32 rate: SMs x 128 FMA lanes x 2 FLOP x the maximum SM clock (nominal, not measured)."""
+    import torch
+
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def _l2_bytes() -> int:
@@ -734,7 +748,7 @@ def measure_workload(name: str, stream, peaks: dict, reps: int = 20) -> dict:
 
     from paged_kv_cache_181_gb300 import _lib, configs, workload
 
-    w = configs.ALL[name]
+    w = (configs.ALL | configs.VARIANTS)[name]
     dev = torch.device("cuda", torch.cuda.current_device())
     case = workload.build_case(w, device=dev, layers=1, data_device=dev)
     flops = 4 * w.head_dim * w.num_heads * visible_pairs(case.meta)
@@ -762,11 +776,13 @@ def measure_workload(name: str, stream, peaks: dict, reps: int = 20) -> dict:
     del flush
     ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
     tflops = flops / (ms * 1e-3) / 1e12
+    att_peak = {"frac_of_burst": tflops / peaks["bf16_tflops"],
+                "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"]} if w.dtype != "f32" else {
+        "frac_of_fp32_fma": tflops / fp32_fma_peak_tflops(),
+        "peak_note": "fp32 runs on the CUDA cores: the denominator is the nominal fp32 FMA rate"}
     res = {
         "attention": {"api": "paged_kv_write_attn (fused write + attention), one layer", "ms_per_call": ms,
-                      "algorithmic_flops_per_call": flops, "tflops": tflops,
-                      "frac_of_burst": tflops / peaks["bf16_tflops"],
-                      "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+                      "algorithmic_flops_per_call": flops, "tflops": tflops} | att_peak | {
                       "launches_per_call": launches, "split_plan": {"splits": plan[0], "whole_items": plan[1]},
                       "l2": "flushed before each timed call", "dtype": w.dtype},
         "kv_write": wr | {"frac_of_hbm": wr["gbs"] / peaks["hbm_gbs"]},

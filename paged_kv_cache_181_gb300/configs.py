@@ -94,7 +94,18 @@ LONG_WINDOW = Workload(
     notes="kv_len 26520 (last block half written); 1700 blocks per branch per layer pool",
 )
 
+# The long window's shapes with fp32 inputs, one layer: the CUDA-core kernel at full size.
+LONG_WINDOW_F32 = Workload(
+    name="long-window-f32-1L", dtype="f32", batch=2, num_heads=40, num_kv_heads=40, head_dim=128,
+    block_size=16, chunk_tokens=1560, window_chunks=16, sink_chunks=1, history_tokens=16 * 1560,
+    query_tokens=1560, action_len=0, pool_blocks=2 * 1700, sigma=1.0, seed=7, layers=1,
+    notes="the long-window geometry in fp32 (one layer)",
+)
+
 ALL = {w.name: w for w in (TINY, ONE_FRAME, ONE_FRAME_PARTIAL, GQA_ACTION, MIXED_MASK, LONG_WINDOW)}
+
+# Measured by the benchmark beside the workloads above (same geometry, another input dtype).
+VARIANTS = {w.name: w for w in (LONG_WINDOW_F32,)}
 
 
 # ---------------------------------------------------------------- packed heterogeneous rows
