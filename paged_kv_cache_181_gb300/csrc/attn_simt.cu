@@ -451,6 +451,9 @@ PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
 // decoded as the kernel decodes it.
 template <typename T>
 __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
+  // Launched as a programmatic dependent of the attention launch (it may be scheduled while the attention
+  // drains): wait here until that grid has completed and its partial results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t wi = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   int64_t item = wi;  // token * Hq + head
@@ -526,10 +529,23 @@ int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
   }
   if (warps <= 0) return 0;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  // Programmatic dependent launch: the combine's launch overlaps the attention's last CTAs; the kernel's
+  // first instruction waits for the attention grid (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaErrorInvalidValue;
   switch (dt) {
-    case PKV_F32: attn_combine_kernel<float><<<grid, 256, 0, s>>>(a); break;
-    case PKV_BF16: attn_combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a); break;
-    case PKV_F16: attn_combine_kernel<__half><<<grid, 256, 0, s>>>(a); break;
+    case PKV_F32: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<float>, a); break;
+    case PKV_BF16: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<__nv_bfloat16>, a); break;
+    case PKV_F16: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<__half>, a); break;
   }
-  return (int)cudaGetLastError();
+  return (int)e;
 }

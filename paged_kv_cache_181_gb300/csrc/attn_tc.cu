@@ -229,6 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = a.Hq / a.Hkv;
+  // The split tail's combine (a programmatic dependent launch) may be scheduled once every CTA of this
+  // grid is running; it waits for this grid's completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // CTA -> (group member gi, tile pair, kv head, row): the CTAs of one (row, kv head) are
   // adjacent in launch order, so they run together and share its keys and values in L2.
   // (Issuing the odd last tiles of every head after all pairs, to fill the last wave with
