@@ -13,7 +13,9 @@
 //   S = Q K^T  thread (ty, tx) owns rows ty + 16i and keys tx + 16j (i, j < 4):
 //              per 4 dimensions it loads 4 query and 4 key float4s and does 64
 //              FMAs (rows and keys interleaved by 16, so a warp's key loads hit
-//              distinct banks and its query loads are broadcasts);
+//              distinct banks and its query loads are broadcasts); the next 4
+//              dimensions' operands are loaded while these FMAs run (two warps
+//              per SM partition cannot hide shared-memory latency otherwise);
 //   softmax    each row's 64 scores sit in the 16 threads of one half-warp:
 //              maxima and sums by shuffles; P goes to shared memory transposed;
 //   O += P V   thread (ty, tx) owns rows 4ty..4ty+3 and columns 4tx + 64c:
@@ -253,17 +255,26 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
-#pragma unroll 4
-    for (int d = 0; d < D; d += 4) {
-      float4 qv[4], kv[4];
+    {
+      float4 qv[2][4], kv[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d);
+      for (int i = 0; i < 4; ++i) qv[0][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kv[j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d);
+      for (int j = 0; j < 4; ++j) kv[0][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int d = 0; d < D; d += 4) {
+        const int cur = (d >> 2) & 1, nxt = cur ^ 1;
+        if (d + 4 < D) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] = dot4(qv[i], kv[j], s[i][j]);
+          for (int i = 0; i < 4; ++i) qv[nxt][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d + 4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) kv[nxt][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d + 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s[i][j] = dot4(qv[cur][i], kv[cur][j], s[i][j]);
+      }
     }
     // Online softmax per row: the row's 64 scores live in this half-warp (lanes with the same ty).
 #pragma unroll
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < 4 * NC; ++c) acc[i][c] *= alr[i];
-#pragma unroll 4
+#pragma unroll 8
       for (int k = 0; k < kSK; ++k) {
         const float4 pv = *reinterpret_cast<const float4*>(p_s + k * PL + 4 * ty);
         const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
