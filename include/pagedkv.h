@@ -250,13 +250,14 @@ PKV_API pkv_status paged_kv_gather(const void* key_pool, const void* value_pool,
  * fits.  Tq = total query tokens; 0 for empty sizes.  A smaller workspace
  * makes a planned split count shrink to what fits.
  *
- * Planning: the tensor-core kernel runs one CTA per item (256 queries of one
- * row and head).  When the items fill the SMs a whole number of times plus a
- * partial last wave, the whole waves run unsplit and only the last wave's
- * items split their key range, into the count that minimises that wave's
- * estimated time; a second, combine launch merges their partials.  Forced
- * splits (PKV_SPLITS) split every item.  The CUDA-core kernel splits all of its
- * items or none.  pkv_last_split_plan reports what the last call chose.
+ * Planning: each kernel runs one CTA per item (256 queries of one row and
+ * head for the tensor-core kernel, 64 for the CUDA-core one).  When the items
+ * fill the SMs a whole number of times plus a partial last wave, the whole
+ * waves run unsplit and only the last wave's items split their key range, into
+ * the count that minimises that wave's estimated time; a second, combine launch
+ * merges their partials.  With fewer items than SMs every item splits.  Forced
+ * splits (PKV_SPLITS) split every item.  pkv_last_split_plan reports what the
+ * last call chose.
  */
 PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int max_query_len, int max_seq_len);
 

@@ -98,11 +98,29 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
   int* lim_s = reinterpret_cast<int*>(m_s + kSQ);  // [kSQ], then the CTA's largest limit
   int* kv_hi_s = lim_s + kSQ;
 
+  // CTA -> (row, query tile, head, key-range split).  Without a split tail the grid is (rows x
+  // query tiles, heads, splits).  With one it is one-dimensional over the items in the same order
+  // (query tiles fastest, then rows, then heads: the CTAs of one row and head run together and
+  // share its keys in L2): items [0, split_direct) run whole, every later item takes num_splits
+  // consecutive CTAs.
   const int tiles_per_row = (a.max_query_len + kSQ - 1) / kSQ;
-  const int b = blockIdx.x / tiles_per_row;
-  const int tile = blockIdx.x % tiles_per_row;
-  const int h = blockIdx.y;
-  const int split = blockIdx.z;
+  int x = blockIdx.x, h = blockIdx.y, split = blockIdx.z, nsplit = a.num_splits;
+  if (a.split_direct > 0) {
+    int u = blockIdx.x;
+    split = 0;
+    nsplit = 1;
+    if (u >= a.split_direct) {
+      const int p = u - a.split_direct;
+      u = a.split_direct + p / a.num_splits;
+      split = p % a.num_splits;
+      nsplit = a.num_splits;
+    }
+    const int row_items = a.B * tiles_per_row;
+    h = u / row_items;
+    x = u % row_items;
+  }
+  const int b = x / tiles_per_row;
+  const int tile = x % tiles_per_row;
   const int kvh = h / (a.Hq / a.Hkv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ty = tid >> 4, tx = tid & 15;
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
 
   // This split's range of key tiles.
   const int n_tiles = (kv_hi + kSK - 1) / kSK;
-  const int per = (n_tiles + a.num_splits - 1) / a.num_splits;
+  const int per = (n_tiles + nsplit - 1) / nsplit;
   const int t_begin = split * per;
   const int t_end = min(n_tiles, t_begin + per);
 
@@ -270,10 +288,23 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
 #pragma unroll
           for (int j = 0; j < 4; ++j) kv[nxt][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d + 4);
         }
+        // Component by component: 16 independent FMAs between two on the same score.
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[i][j] = dot4(qv[cur][i], kv[cur][j], s[i][j]);
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].x, kv[cur][j].x, s[i][j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].y, kv[cur][j].y, s[i][j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].z, kv[cur][j].z, s[i][j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].w, kv[cur][j].w, s[i][j]);
       }
     }
     // Online softmax per row: the row's 64 scores live in this half-warp (lanes with the same ty).
@@ -321,21 +352,35 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < 4 * NC; ++c) acc[i][c] *= alr[i];
-#pragma unroll 8
-      for (int k = 0; k < kSK; ++k) {
-        const float4 pv = *reinterpret_cast<const float4*>(p_s + k * PL + 4 * ty);
+      // Two keys per step: the next key's P and V are loaded while this key's FMAs run.
+      float4 p0 = *reinterpret_cast<const float4*>(p_s + 4 * ty), p1;
+      float4 v0[NC], v1[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) v0[c] = *reinterpret_cast<const float4*>(v_s + 4 * tx + 64 * c);
+      auto pv_fma = [&](const float4& pv, const float4 (&vv)[NC]) {
         const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const float4 vv = *reinterpret_cast<const float4*>(v_s + k * LD + 4 * tx + 64 * c);
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            acc[i][4 * c + 0] = fmaf(pr[i], vv.x, acc[i][4 * c + 0]);
-            acc[i][4 * c + 1] = fmaf(pr[i], vv.y, acc[i][4 * c + 1]);
-            acc[i][4 * c + 2] = fmaf(pr[i], vv.z, acc[i][4 * c + 2]);
-            acc[i][4 * c + 3] = fmaf(pr[i], vv.w, acc[i][4 * c + 3]);
+            acc[i][4 * c + 0] = fmaf(pr[i], vv[c].x, acc[i][4 * c + 0]);
+            acc[i][4 * c + 1] = fmaf(pr[i], vv[c].y, acc[i][4 * c + 1]);
+            acc[i][4 * c + 2] = fmaf(pr[i], vv[c].z, acc[i][4 * c + 2]);
+            acc[i][4 * c + 3] = fmaf(pr[i], vv[c].w, acc[i][4 * c + 3]);
           }
+      };
+#pragma unroll 4
+      for (int k = 0; k < kSK; k += 2) {
+        p1 = *reinterpret_cast<const float4*>(p_s + (k + 1) * PL + 4 * ty);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) v1[c] = *reinterpret_cast<const float4*>(v_s + (k + 1) * LD + 4 * tx + 64 * c);
+        pv_fma(p0, v0);
+        if (k + 2 < kSK) {
+          p0 = *reinterpret_cast<const float4*>(p_s + (k + 2) * PL + 4 * ty);
+#pragma unroll
+          for (int c = 0; c < NC; ++c) v0[c] = *reinterpret_cast<const float4*>(v_s + (k + 2) * LD + 4 * tx + 64 * c);
         }
+        pv_fma(p1, v1);
       }
     }
   }
@@ -358,7 +403,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
     const int64_t tok = (int64_t)q0 + qi;
     const float lr = l_s[r];
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
-    if (a.num_splits == 1) {
+    if (nsplit == 1) {
       T* o = (T*)a.out + (tok * a.Hq + h) * D;
 #pragma unroll
       for (int c = 0; c < NC; ++c)
@@ -458,8 +503,8 @@ PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
 }
 
 // One warp per combined (token, head) row.  With a split tail (split_direct > 0) only the split
-// items' rows are combined: warp w takes row wi % rows of tensor-core item split_direct + wi / rows,
-// decoded as the kernel decodes it.
+// items' rows are combined: warp w takes row wi % rows of item split_direct + wi / rows, decoded as
+// the kernel that ran decodes it.
 template <typename T>
 __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
   // Launched as a programmatic dependent of the attention launch (it may be scheduled while the attention
@@ -469,20 +514,33 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
   const int lane = threadIdx.x & 31;
   int64_t item = wi;  // token * Hq + head
   if (a.split_direct > 0) {
-    const int rows = a.max_query_len < kTcItemRows ? a.max_query_len : kTcItemRows;
-    const int g = a.Hq / a.Hkv;
-    const int n_qp = (a.max_query_len + kTcItemRows - 1) / kTcItemRows;
-    const int64_t items = (int64_t)a.B * a.Hq * n_qp;
+    const int unit = a.simt_items ? kSimtItemRows : kTcItemRows;
+    const int rows = a.max_query_len < unit ? a.max_query_len : unit;
+    const int n_q = (a.max_query_len + unit - 1) / unit;
+    const int64_t items = (int64_t)a.B * a.Hq * n_q;
     const int64_t u = a.split_direct + wi / rows;
     if (u >= items) return;
-    const PkvTcItem it = pkv_tc_item((int)u, g, n_qp, a.Hkv);
-    const int i = it.qp * kTcItemRows + (int)(wi % rows);
-    const int q0 = a.query_start_loc[it.b];
-    int Sq = a.query_start_loc[it.b + 1] - q0;
+    int b, h, qt;
+    if (a.simt_items) {
+      const int64_t row_items = (int64_t)a.B * n_q;
+      h = (int)(u / row_items);
+      const int x = (int)(u % row_items);
+      b = x / n_q;
+      qt = x % n_q;
+    } else {
+      const int g = a.Hq / a.Hkv;
+      const PkvTcItem it = pkv_tc_item((int)u, g, n_q, a.Hkv);
+      b = it.b;
+      h = it.kvh * g + it.gi;
+      qt = it.qp;
+    }
+    const int i = qt * unit + (int)(wi % rows);
+    const int q0 = a.query_start_loc[b];
+    int Sq = a.query_start_loc[b + 1] - q0;
     Sq = Sq < 0 ? 0 : (Sq > a.max_query_len ? a.max_query_len : Sq);
     const int64_t tok = (int64_t)q0 + i;
     if (i >= Sq || tok < 0 || tok >= a.Tq) return;
-    item = tok * a.Hq + it.kvh * g + it.gi;
+    item = tok * a.Hq + h;
   } else if (item >= a.Tq * a.Hq) {
     return;
   }
@@ -509,6 +567,12 @@ int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
   }
   const int tiles_per_row = (a.max_query_len + kSQ - 1) / kSQ;
   dim3 grid((unsigned)(a.B * tiles_per_row), (unsigned)a.Hq, (unsigned)a.num_splits);
+  if (a.split_direct > 0) {
+    const int64_t items = (int64_t)a.B * tiles_per_row * a.Hq;
+    const int64_t ctas = a.split_direct + (items - a.split_direct) * a.num_splits;
+    if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;  // the planner keeps it below
+    grid = dim3((unsigned)ctas);
+  }
   attn_simt_kernel<T, D><<<grid, kSThreads, smem, s>>>(a);
   return (int)cudaGetLastError();
 }
@@ -534,9 +598,10 @@ int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   int64_t warps = a.Tq * a.Hq;
   if (a.split_direct > 0) {
-    const int64_t n_qp = (a.max_query_len + kTcItemRows - 1) / kTcItemRows;
-    const int64_t rows = a.max_query_len < kTcItemRows ? a.max_query_len : kTcItemRows;
-    warps = ((int64_t)a.B * a.Hq * n_qp - a.split_direct) * rows;
+    const int64_t unit = a.simt_items ? kSimtItemRows : kTcItemRows;
+    const int64_t n_q = (a.max_query_len + unit - 1) / unit;
+    const int64_t rows = a.max_query_len < unit ? a.max_query_len : unit;
+    warps = ((int64_t)a.B * a.Hq * n_q - a.split_direct) * rows;
   }
   if (warps <= 0) return 0;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);

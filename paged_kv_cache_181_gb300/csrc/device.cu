@@ -175,12 +175,14 @@ struct SplitPlan {
 // tiles' time), plus the combine at about 0.3 tiles per split.  Fit to one row x 8 heads x 256
 // queries over 26520 keys: 354 / 193 / 113 / 73 / 61 us for 1 / 2 / 4 / 8 / 16 splits.  (Splitting
 // every item of a full grid only adds fixed costs: 2 splits cost +8 % on the long-window workload.)
-SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits, bool tail_ok) {
+// The CUDA-core kernel uses the same estimate; its fixed cost is well under one of its slower
+// 64-key tiles, so the estimate errs towards fewer splits there.
+SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits) {
   const SplitPlan none{1, items};
   if (items <= 0 || tiles <= 1 || sms <= 0) return none;
   const int64_t full = items / sms;
   const int64_t tail = items - full * sms;
-  if (tail == 0 || (full > 0 && !tail_ok)) return none;
+  if (tail == 0) return none;
   int best = 1;
   double best_cost = (double)(tiles + 8);
   for (int s = 2; s <= max_splits; ++s) {
@@ -200,15 +202,16 @@ SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits, boo
 
 // Key-range splits the call plans from host-visible sizes.  An item is what one CTA of the
 // unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 64 for the
-// CUDA-core one.  Only the tensor-core kernel splits a tail behind whole items; the CUDA-core
-// kernel splits all of its items or none (only when they leave SMs idle).
+// CUDA-core one.  Both kernels split only the tail behind whole waves (every item when there
+// are fewer items than CTA slots).  The CUDA-core kernel's tail runs as a one-dimensional grid,
+// whose size must stay a valid grid dimension.
 static SplitPlan planned_splits(int B, int Hq, int max_query_len, int max_seq_len, bool tc, int sms) {
   const int64_t q_unit = tc ? kTcItemRows : kSimtItemRows;
   const int64_t k_tile = tc ? 128 : kSimtKeyTile;
   const int64_t items = (int64_t)B * Hq * ((max_query_len + q_unit - 1) / q_unit);
   const int64_t tiles = ((int64_t)max_seq_len + k_tile - 1) / k_tile;
-  SplitPlan p = plan_splits(items, tiles, tc ? sms : sms * kSimtCtasPerSm, kMaxSplits, tc);
-  if (!tc) p.direct = 0;
+  SplitPlan p = plan_splits(items, tiles, tc ? sms : sms * kSimtCtasPerSm, kMaxSplits);
+  if (!tc && p.direct > 0 && p.direct + (items - p.direct) * p.splits > 0x7fffffff) p = SplitPlan{1, items};
   return p;
 }
 
@@ -344,9 +347,13 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
   int rc = -1;
   if (use_tc) rc = pkv_launch_attn_tc(a, dt, stream);
   if (rc == -1) {
-    // The CUDA-core kernel splits every item or none: its combine merges every row.
-    a.split_direct = 0;
-    pkv_set_split_plan(splits, 0);
+    // Planned for the tensor-core kernel, which declined: the CUDA-core kernel splits every item
+    // instead (its combine then merges every row).  Planned for the CUDA-core kernel: its own tail.
+    if (use_tc) {
+      a.split_direct = 0;
+      pkv_set_split_plan(splits, 0);
+    }
+    a.simt_items = 1;
     rc = pkv_launch_attn_simt(a, dt, stream);
   }
   if (rc != 0) return pkv_fail(PKV_ERR_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString((cudaError_t)rc));

@@ -51,10 +51,14 @@ struct PkvAttnArgs {
   int B, W, Hq, Hkv, D;
   int max_query_len, max_seq_len;
   int num_splits;
-  // Tensor-core grid with a split tail (num_splits > 1): items [0, split_direct) run one CTA
-  // each and write `out`; every later item runs num_splits CTAs over parts of its key range
-  // and leaves partials for the combine.  0: every item is split (the CUDA-core kernel).
+  // Split tail (num_splits > 1): items [0, split_direct) run one CTA each and write `out`;
+  // every later item runs num_splits CTAs over parts of its key range and leaves partials for
+  // the combine.  0: every item is split.
   int split_direct;
+  // Which kernel's items the split tail counts: 0 the tensor-core kernel's (256 queries of one
+  // row and head, pkv_tc_item order), 1 the CUDA-core kernel's (64 queries; the row's query
+  // tiles fastest, then the rows, then the heads).
+  int simt_items;
   int check;
   int contiguous;  // PKV_CONTIGUOUS_KV
   float scale;

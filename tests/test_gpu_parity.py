@@ -205,9 +205,16 @@ def test_split_tail_shrinks_to_the_workspace(lib):
     assert splits == 2 and whole == sms and launches == 2, (splits, whole, launches)
 
 
+def _simt_whole_items(w, sms):
+    """Items the CUDA-core kernel runs whole: its whole waves of 64-query items (one CTA per SM)."""
+    items = w.batch * w.num_heads * -(-w.q_len // 64)
+    return items // sms * sms, items
+
+
 def test_negative_scale_plans_for_the_kernel_that_runs(lib):
     """A negative softmax scale on bf16 is refused unless the CUDA-core kernel is asked for by name; then it
-    runs there, with that kernel's split plan (no whole items), and matches the oracle."""
+    runs there, with that kernel's split plan (its own 64-query items: 4 whole waves and a split tail of
+    32), and matches the oracle."""
     from paged_kv_cache_181_gb300 import workload
 
     w = _tail_workload()
@@ -218,4 +225,36 @@ def test_negative_scale_plans_for_the_kernel_that_runs(lib):
     assert e.value.status == lib.PKV_ERR_UNSUPPORTED and lib.last_launches() == 0
     del case
     launches, (splits, whole) = _run_tail(lib, w, False, scale_sign=-1.0, flags=lib.PKV_FORCE_SIMT)
-    assert whole == 0, (splits, whole)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want_whole, items = _simt_whole_items(w, sms)
+    assert items > want_whole > 0 and whole == want_whole and splits > 1 and launches == 2, (splits, whole)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two-call", "fused"])
+def test_cuda_core_split_tail_long_window_f32(lib, fused):
+    """fp32 at the long window's full size: 2000 CUDA-core items of 64 queries are 13 waves of 152 SMs and
+    24 more; those 24 split their 415 key tiles and the combine merges them, the rest run whole.  Sampled
+    rows of every (row, head) -- the tail's included -- against the float64 oracle."""
+    from paged_kv_cache_181_gb300 import workload
+
+    w = configs.LONG_WINDOW_F32
+    case = workload.build_case(w, poison=True, keep_draws=True, layers=1)
+    if fused:
+        out = case.write_attend(0, flags=lib.PKV_CHECK_BOUNDS)
+    else:
+        case.write(0, lib.PKV_CHECK_BOUNDS)
+        out = case.attend(0, lib.PKV_CHECK_BOUNDS)
+    launches, (splits, whole) = lib.last_launches(), lib.last_split_plan()
+    torch.cuda.synchronize()
+    assert lib.check() == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want_whole, items = _simt_whole_items(w, sms)
+    if items % sms:
+        assert whole == want_whole and splits > 1 and launches == 2, (splits, whole, launches)
+    oc = cases.oracle_metadata(w)
+    cases.oracle_pools(w, case.draws[0], oc)
+    sample = cases.sample_rows(w, 12)
+    want = cases.expected(w, oc, sample)
+    max_abs, mean_abs = cases.compare(out.float().cpu().numpy(), want, w.dtype, ~np.isnan(want))
+    tol_max, tol_mean = cases.TOL[w.dtype]
+    assert max_abs <= tol_max and mean_abs <= tol_mean, (max_abs, mean_abs)
