@@ -491,7 +491,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(result), flush=True)
 
 
-KERNEL_REV = "tc-v15"
+KERNEL_REV = "tc-v16"
 
 
 def measure_graph(case, steps: int, fused: bool, main_ms_step: float) -> dict:

@@ -90,6 +90,7 @@ struct Cfg {
   static constexpr int TILE = BN * D * 2;          // one key or value tile
   static constexpr int NSLOT = D == 128 ? 5 : 10;  // ring slots (fits 227 KB with both query tiles)
   static constexpr int GS = (D / 64) * 1024;       // stride of 8-row atoms in a key/value tile
+  static constexpr int PART_ROW = D * 4 + 16;      // staged fp32 partial row (padded: conflict-free)
 };
 
 template <int D>
@@ -603,8 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue
     // A full query tile of a one-split call leaves through shared memory (the Q buffer, free once
     // every MMA is done) and TMA stores: one head's rows are Hq*D apart in the output, so rows
-    // stored thread by thread scatter.  The other tiles store per thread.  `staged` is the same
-    // for every thread of the warpgroup, which meets at a named barrier.
+    // stored thread by thread scatter.  A split's fp32 partials are staged too (below); a ragged
+    // tile of a whole item stores per thread.  `staged` and `whole_out` are the same for every
+    // thread of the warpgroup, which meets at a named barrier.
     const bool whole_out = a.num_splits == 1 || (int)blockIdx.x < a.split_direct;
     const bool staged = whole_out && n > 0 && i0 + grp * BM + BM <= Sq;
     float o[D];
@@ -659,10 +661,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::bulk_commit();
         ptx::bulk_wait_read_all();  // shared memory read before the CTA (and its shared memory) goes away
       }
+    } else if (!whole_out) {
+      // A split's fp32 partial rows (D*4 bytes each, Hq*D*4 apart): stored thread by thread, each
+      // warp instruction would touch 32 rows.  They go through shared memory instead -- the key/value
+      // ring, which no copy or MMA uses once mma_done has completed -- and each warp then stores whole
+      // rows, one per instruction.
+      // Staged at the query's row of the tile (a lone M = 64 tile's rows sit in lanes 0-15).
+      uint8_t* st = sm.kv[0] + grp * (BM * C::PART_ROW);
+      if (ok && valid && !sm.abort) {
+        uint8_t* srow = st + (i - (i0 + grp * BM)) * C::PART_ROW;
+#pragma unroll
+        for (int v4 = 0; v4 < D / 4; ++v4)
+          *reinterpret_cast<float4*>(srow + v4 * 16) =
+              n > 0 ? make_float4(o[v4 * 4] * inv, o[v4 * 4 + 1] * inv, o[v4 * 4 + 2] * inv, o[v4 * 4 + 3] * inv)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(BM) : "memory");
+      const int sp = ((int)blockIdx.x - a.split_direct) % a.num_splits;
+      if (ok && valid) {
+        // natural-log log-sum-exp of this split: ln 2 * (m_ref + log2 l)
+        a.part_lse[((int64_t)sp * a.Tq + tok) * a.Hq + h] =
+            (n > 0 && l > 0.f) ? 0.6931471805599453f * (m_ref + __log2f(l)) : -INFINITY;
+      }
+      if (!sm.abort) {
+        constexpr int V4 = D / 4;                           // 16-byte pieces per row
+        const int row_lim = min(BM, Sq - (i0 + grp * BM));  // rows of this tile that are queries
+        for (int e = quarter * 32 + lane; e < BM * V4; e += 128) {
+          const int r = e / V4, v4 = e % V4;
+          if (r >= row_lim) break;
+          const int64_t t = (int64_t)q0 + i0 + grp * BM + r;
+          reinterpret_cast<float4*>(a.part_o + (((int64_t)sp * a.Tq + t) * a.Hq + h) * D)[v4] =
+              *reinterpret_cast<const float4*>(st + r * C::PART_ROW + v4 * 16);
+        }
+      }
     } else if (ok) {
       if (!valid) {
         // query row past the end of this row's queries: nothing to store
-      } else if (whole_out) {
+      } else {
         uint4* dst = reinterpret_cast<uint4*>((uint16_t*)a.out + (tok * a.Hq + h) * D);
 #pragma unroll
         for (int v8 = 0; v8 < D / 8; ++v8) {
@@ -675,17 +710,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           dst[v8] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-      } else {
-        const int sp = ((int)blockIdx.x - a.split_direct) % a.num_splits;
-        float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)sp * a.Tq + tok) * a.Hq + h) * D);
-#pragma unroll
-        for (int v4 = 0; v4 < D / 4; ++v4) {
-          dst[v4] = n > 0 ? make_float4(o[v4 * 4] * inv, o[v4 * 4 + 1] * inv, o[v4 * 4 + 2] * inv, o[v4 * 4 + 3] * inv)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // natural-log log-sum-exp of this split: ln 2 * (m_ref + log2 l)
-        a.part_lse[((int64_t)sp * a.Tq + tok) * a.Hq + h] =
-            (n > 0 && l > 0.f) ? 0.6931471805599453f * (m_ref + __log2f(l)) : -INFINITY;
       }
     }
   }
