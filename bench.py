@@ -223,8 +223,9 @@ def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int | None = None, r
         if budget_s is not None and time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    what = (f"all {rows} rows x {w1.num_heads} heads" if done == len(units) and n_heads == w1.num_heads
-            else f"{done} of {rows * w1.num_heads} (row, head) pairs")
+    row_txt = "row 0" if rows == 1 else f"rows 0-{rows - 1}"
+    what = (f"{row_txt}, all {w1.num_heads} heads" if done == len(units) and n_heads == w1.num_heads
+            else f"{row_txt}, {done} of {rows * w1.num_heads} (row, head) pairs")
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
             "sample": f"{w.name}: layer 0, {what}, {w1.q_len} queries x {int(oc.seq_lens[0])} keys each, "
                       f"float32 NumPy oracle ({dt:.1f} s)", "seconds": dt}
