@@ -19,7 +19,10 @@
 //   softmax    each row's 64 scores sit in the 16 threads of one half-warp:
 //              maxima and sums by shuffles; P goes to shared memory transposed;
 //   O += P V   thread (ty, tx) owns rows 4ty..4ty+3 and columns 4tx + 64c:
-//              per key one float4 of P and D/64 float4s of V for 16 D/64 FMAs.
+//              per key one float4 of P and D/64 float4s of V for 16 D/64 FMAs,
+//              the next key's operands loaded while these FMAs run.
+// Like the tensor-core grid, the grid splits the key ranges of only its last,
+// partly filled wave of items (every item when there are fewer than SMs).
 
 #include <math.h>
 #include <string.h>
@@ -75,13 +78,6 @@ PKV_DEVINLINE void store4(T* p, float x0, float x1, float x2, float x3) {
     memcpy(&u, t, sizeof(u));
     *reinterpret_cast<uint2*>(p) = u;
   }
-}
-
-PKV_DEVINLINE float dot4(float4 a, float4 b, float acc) {
-  acc = fmaf(a.x, b.x, acc);
-  acc = fmaf(a.y, b.y, acc);
-  acc = fmaf(a.z, b.z, acc);
-  return fmaf(a.w, b.w, acc);
 }
 
 template <typename T, int D>
