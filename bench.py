@@ -818,7 +818,8 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     landed, and each layer's output is copied device -> host on a third stream as soon as it is ready.
     Alternate steps use two device copies of the inputs and outputs, so that a step's uploads never wait
     for the previous step's compute of the same layer (uploads run slower while the attention runs on
-    some machines; with one copy that coupled the two streams layer by layer).
+    some machines; with one copy that coupled the two streams layer by layer), and a step's last read-backs
+    overlap the next step's first layers.  Every copy of every timed step is inside the timed region.
     """
     import torch
 
@@ -861,7 +862,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     # compute itself slowed down or waited for its inputs.
     cp_t = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
 
-    def e2e_step():
+    def e2e_step(last: bool = True):
         k = step_no[0] % 2
         step_no[0] += 1
         q_d, k_d, v_d, o_d = io_sets[k]
@@ -904,7 +905,8 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
                 host_out[l].copy_(o_d[l], non_blocking=True)
                 fetched[k][l].record(down)
         meta_free[k].record(stream)
-        stream.wait_stream(down)
+        if last:  # the timed region ends with every output on the host
+            stream.wait_stream(down)
 
     for ev in fetched[0] + fetched[1] + computed[0] + computed[1] + meta_free:
         ev.record(stream)
@@ -936,8 +938,10 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
     with ClockSampler(gpu_index) as clk:  # clocks while copies and compute overlap (power draw differs)
         start.record(stream)
         up.wait_event(start)  # no upload of the timed steps starts before the clock does
-        for _ in range(steps):
-            e2e_step()
+        # Steps are pipelined: a step's last read-backs overlap the next step's first layers (its output
+        # buffers are the other set's); the last step ends with every read-back done.
+        for i in range(steps):
+            e2e_step(last=i == steps - 1)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
