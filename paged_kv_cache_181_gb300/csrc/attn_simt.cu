@@ -442,18 +442,19 @@ PKV_DEVINLINE void store_lane(T* dst, const float* v) {
 
 // One (token, head) row by one warp: O = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M).  Lane l
 // holds columns [l NC, l NC + NC) (NC = D / 32) and reads them as one vector per split; lane s reads
-// split s's log-sum-exp (at most 32 splits).  The first eight splits' rows are loaded together with
-// the log-sum-exps, so a row with up to eight splits costs one round trip to memory.
-template <typename T, int NC>
+// split s's log-sum-exp (at most 32 splits).  The first kBatch splits' rows are loaded together with
+// the log-sum-exps, so a row of up to kBatch splits costs one round trip to memory (the launch picks
+// kBatch = 8 or 16 from the split count: the larger batch holds twice the registers).
+template <typename T, int NC, int kBatch>
 PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
   using V = typename std::conditional<NC == 4, float4, float2>::type;
   const int S = a.num_splits;
   const int64_t stride = a.Tq * a.Hq;  // rows between splits
   const float* base = a.part_o + item * (32 * NC) + lane * NC;
-  float x[8][NC];
+  float x[kBatch][NC];
   auto load = [&](int s0) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       V v;
       if (s0 + u < S)
         v = __ldg(reinterpret_cast<const V*>(base + (int64_t)(s0 + u) * stride * (32 * NC)));
@@ -483,12 +484,12 @@ PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   for (int s0 = 0;;) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       const float ws = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
 #pragma unroll
       for (int c = 0; c < NC; ++c) acc[c] = fmaf(s0 + u < S ? ws : 0.f, x[u][c], acc[c]);
     }
-    s0 += 8;
+    s0 += kBatch;
     if (s0 >= S) break;
     load(s0);
   }
@@ -501,7 +502,7 @@ PKV_DEVINLINE void combine_row(const PkvAttnArgs& a, int64_t item, int lane) {
 // One warp per combined (token, head) row.  With a split tail (split_direct > 0) only the split
 // items' rows are combined: warp w takes row wi % rows of item split_direct + wi / rows, decoded as
 // the kernel that ran decodes it.
-template <typename T>
+template <typename T, int kBatch>
 __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
   // Launched as a programmatic dependent of the attention launch (it may be scheduled while the attention
   // drains): wait here until that grid has completed and its partial results are visible.
@@ -541,9 +542,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
     return;
   }
   if (a.D == 128)
-    combine_row<T, 4>(a, item, lane);
+    combine_row<T, 4, kBatch>(a, item, lane);
   else
-    combine_row<T, 2>(a, item, lane);
+    combine_row<T, 2, kBatch>(a, item, lane);
 }
 
 template <typename T, int D>
@@ -614,10 +615,20 @@ int pkv_launch_attn_combine(const PkvAttnArgs& a, pkv_dtype dt, void* stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaErrorInvalidValue;
+  const bool wide = a.num_splits > 8;
   switch (dt) {
-    case PKV_F32: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<float>, a); break;
-    case PKV_BF16: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<__nv_bfloat16>, a); break;
-    case PKV_F16: e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<__half>, a); break;
+    case PKV_F32:
+      e = wide ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<float, 16>, a)
+               : cudaLaunchKernelEx(&cfg, attn_combine_kernel<float, 8>, a);
+      break;
+    case PKV_BF16:
+      e = wide ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<__nv_bfloat16, 16>, a)
+               : cudaLaunchKernelEx(&cfg, attn_combine_kernel<__nv_bfloat16, 8>, a);
+      break;
+    case PKV_F16:
+      e = wide ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<__half, 16>, a)
+               : cudaLaunchKernelEx(&cfg, attn_combine_kernel<__half, 8>, a);
+      break;
   }
   return (int)e;
 }

@@ -122,6 +122,20 @@ def test_noalloc_planned_splits(lib):
             check_against_oracle(c, got, dtype)
 
 
+def test_noalloc_cuda_core_split_tail(lib):
+    # fp32 runs on the CUDA-core kernel, whose items are 64 queries: 8 heads x 1280 queries = 160 items, one
+    # wave of 152 SMs and a tail of 8 that splits into the scratch while the rest run whole.
+    c = make_case(8, torch.float32, 8, 8, 64, (1280,), (3000,), ([(1720, 3000)],))
+    ref, got, launches, ref_plan, plan = run_both(lib, c, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    items = 8 * 1280 // 64
+    if items > sms and items % sms:
+        assert plan[0] > 1 and plan[1] == items // sms * sms and launches == 2, (plan, launches)
+    assert plan == ref_plan, (plan, ref_plan)
+    assert np.array_equal(got, ref)
+    check_against_oracle(c, got, torch.float32)
+
+
 def test_noalloc_clamps_forced_splits_like_the_workspace_call(lib):
     # PKV_SPLITS(20) asks for more than the 16 splits either call runs: both take it as 16.
     c = make_case(7, torch.bfloat16, 4, 2, 64, (100,), (3000,), ([(2900, 3000)],))
