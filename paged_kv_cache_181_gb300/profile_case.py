@@ -27,6 +27,8 @@ def main() -> None:
     ap.add_argument("--fused", action="store_true", help="paged_kv_write_attn instead of the two calls")
     ap.add_argument("--packed", default=None, help="run this packed batch's attention call instead (configs.PACKED)")
     ap.add_argument("--gather", action="store_true", help="also stage each layer's window (paged_kv_gather)")
+    ap.add_argument("--dtype", choices=["f32", "bf16", "f16"], default=None,
+                    help="the workload's shapes with this input dtype (f32 runs the CUDA-core kernel)")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="blocks per layer pool (default: the workload's); a smaller pool keeps a capture's device "
                          "memory small without changing the blocks the call reads or writes")
@@ -43,11 +45,13 @@ def main() -> None:
             raise SystemExit(f"device error word 0x{bits:x}")
         print(f"profile_case: {args.packed}, {args.steps} attention call(s): ok")
         return
-    w = configs.ALL[args.workload]
-    if args.pool_blocks:
-        import dataclasses
+    import dataclasses
 
+    w = {**configs.ALL, **configs.VARIANTS}[args.workload]
+    if args.pool_blocks:
         w = dataclasses.replace(w, pool_blocks=args.pool_blocks)
+    if args.dtype:
+        w = dataclasses.replace(w, dtype=args.dtype)
     case = workload.build_case(w, device="cuda", layers=args.layers, data_device="cuda")
     st = case.make_staging() if args.gather else None
     for _ in range(args.steps):
