@@ -251,7 +251,7 @@ PKV_API pkv_status paged_kv_gather(const void* key_pool, const void* value_pool,
  * makes a planned split count shrink to what fits.
  *
  * Planning: each kernel runs one CTA per item (256 queries of one row and
- * head for the tensor-core kernel, 64 for the CUDA-core one).  When the items
+ * head for the tensor-core kernel, 128 for the CUDA-core one).  When the items
  * fill the SMs a whole number of times plus a partial last wave, the whole
  * waves run unsplit and only the last wave's items split their key range, into
  * the count that minimises that wave's estimated time; a second, combine launch

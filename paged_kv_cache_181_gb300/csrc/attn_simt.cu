@@ -8,19 +8,25 @@
 // piecewise_attn.py expressed as a per-query key limit, and an online
 // (running max / running sum) softmax so the key range can be streamed.
 //
-// CTA = 64 queries of one (row, head) and one key-range split; 256 threads as a
+// CTA = 128 queries of one (row, head) and one key-range split; 256 threads as a
 // 16 x 16 grid (ty, tx).  Per 64-key tile, all in fp32 shared memory:
-//   S = Q K^T  thread (ty, tx) owns rows ty + 16i and keys tx + 16j (i, j < 4):
-//              per 4 dimensions it loads 4 query and 4 key float4s and does 64
-//              FMAs (rows and keys interleaved by 16, so a warp's key loads hit
-//              distinct banks and its query loads are broadcasts); the next 4
-//              dimensions' operands are loaded while these FMAs run (two warps
-//              per SM partition cannot hide shared-memory latency otherwise);
+//   S = Q K^T  thread (ty, tx) owns rows ty + 16i (i < 8) and keys tx + 16j
+//              (j < 4): per 4 dimensions it loads 8 query and 4 key float4s and
+//              does 128 FMAs (rows and keys interleaved by 16, so a warp's key
+//              loads hit distinct banks and its query loads are broadcasts);
+//              the next 4 dimensions' operands are loaded while these FMAs run
+//              (two warps per SM partition cannot hide shared-memory latency
+//              otherwise);
 //   softmax    each row's 64 scores sit in the 16 threads of one half-warp:
 //              maxima and sums by shuffles; P goes to shared memory transposed;
-//   O += P V   thread (ty, tx) owns rows 4ty..4ty+3 and columns 4tx + 64c:
-//              per key one float4 of P and D/64 float4s of V for 16 D/64 FMAs,
+//   O += P V   thread (ty, tx) owns rows 8ty..8ty+7 and columns 4tx + 64c:
+//              per key two float4s of P and D/64 float4s of V for 32 D/64 FMAs,
 //              the next key's operands loaded while these FMAs run.
+// The keys come double-buffered (the next tile's arrive during this one), the
+// values single-buffered (a tile's arrive during its scores and softmax): with
+// 8 x 4 scores per thread instead of 4 x 4, the shared-memory wavefronts per FMA
+// fall by a third, and Q, two key tiles, one value tile and P fit in 205 KB
+// for D = 128.
 // Like the tensor-core grid, the grid splits the key ranges of only its last,
 // partly filled wave of items (every item when there are fewer than SMs).
 
@@ -39,12 +45,16 @@ constexpr int kSK = kSimtKeyTile;   // keys per tile
 constexpr int kSThreads = 256;
 constexpr int kSWarps = kSThreads / 32;
 
+constexpr int RI = kSQ / 16;        // query rows per thread (scores: ty + 16i; output: RI*ty + i)
+static_assert(kSQ % 64 == 0 && kSK == 64, "thread tiles assume 64-key tiles and 64k-query CTAs");
+
 template <int D>
 struct SimtSmem {
   static constexpr int LD = D + 4;    // row stride (floats) of Q, K and V: 16-byte rows, staggered banks
   static constexpr int PL = kSQ + 4;  // row stride of P^T
-  // Q, two K/V buffers (the next tile loads while this one is used), P^T, per-row state.
-  static constexpr size_t floats = (size_t)kSQ * LD + (size_t)4 * kSK * LD + (size_t)kSK * PL + 3 * kSQ;
+  // Q, two key buffers (the next tile's keys load while this one is used), one value buffer (a tile's
+  // values load during its scores and softmax), P^T, per-row state.
+  static constexpr size_t floats = (size_t)kSQ * LD + (size_t)3 * kSK * LD + (size_t)kSK * PL + 3 * kSQ;
   static constexpr size_t bytes = floats * sizeof(float) + (kSQ + 1) * sizeof(int);
 };
 
@@ -86,8 +96,9 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
   constexpr int LD = SM::LD, PL = SM::PL, NC = D / 64;
   extern __shared__ __align__(16) float sm[];
   float* q_s = sm;                          // [kSQ][LD]
-  float* kv_buf = q_s + kSQ * LD;           // two buffers of [kSK][LD] keys then [kSK][LD] values
-  float* p_s = kv_buf + 4 * kSK * LD;       // [kSK][PL], P transposed: p_s[key * PL + query]
+  float* k_buf = q_s + kSQ * LD;            // two buffers of [kSK][LD] keys
+  float* v_s = k_buf + 2 * kSK * LD;        // [kSK][LD] values
+  float* p_s = v_s + kSK * LD;              // [kSK][PL], P transposed: p_s[key * PL + query]
   float* alpha_s = p_s + kSK * PL;  // [kSQ] per-tile rescale of each row's O
   float* l_s = alpha_s + kSQ;       // [kSQ]
   float* m_s = l_s + kSQ;           // [kSQ]
@@ -175,7 +186,9 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
   }
   __syncthreads();
   if (warp == 0) {
-    int hi = lim_s[lane] > lim_s[lane + 32] ? lim_s[lane] : lim_s[lane + 32];
+    int hi = 0;
+#pragma unroll
+    for (int r = lane; r < kSQ; r += 32) hi = lim_s[r] > hi ? lim_s[r] : hi;
     hi = __reduce_max_sync(0xffffffffu, hi);
     if (lane == 0) *kv_hi_s = hi;
   }
@@ -190,89 +203,77 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
 
   // Keys at the queries' own positions [cb, ce): read from the new tokens in a fused call.
   const int cb = a.k_new ? base : 0, ce = a.k_new ? base + Sq : 0;
-  const T* kpool = (const T*)a.k_pool;
-  const T* vpool = (const T*)a.v_pool;
 
-  int lim_r[4];
+  int lim_r[RI];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) lim_r[i] = lim_s[ty + 16 * i];
-  float m[4], l[4];  // softmax state of rows ty + 16i (the same in all 16 threads of the half-warp)
+  for (int i = 0; i < RI; ++i) lim_r[i] = lim_s[ty + 16 * i];
+  float m[RI], l[RI];  // softmax state of rows ty + 16i (the same in all 16 threads of the half-warp)
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RI; ++i) {
     m[i] = -INFINITY;
     l[i] = 0.f;
   }
-  float acc[4][4 * NC];  // O rows 4ty + i, columns 4tx + 64c + e
+  float acc[RI][4 * NC];  // O rows RI*ty + i, columns 4tx + 64c + e
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < RI; ++i)
 #pragma unroll
     for (int c = 0; c < 4 * NC; ++c) acc[i][c] = 0.f;
 
-  // Gather 64 keys and values of tile kt through the block table into buffer `buf` (fp32); past
-  // kv_hi: zeros.  fp32 sources go by asynchronous 16-byte copies (the next tile lands while this one
-  // is used); 16-bit ones are loaded and converted.
-  auto gather = [&](int kt, int buf) {
-    float* kd = kv_buf + buf * 2 * kSK * LD;
-    float* vd = kd + kSK * LD;
+  // Gather tile kt's 64 keys (is_v false) or values (true) through the block table into `dst`
+  // (fp32); past kv_hi: zeros.  fp32 sources go by asynchronous 16-byte copies, one commit group per
+  // call; 16-bit ones are loaded and converted.
+  auto gather = [&](int kt, bool is_v, float* dst) {
+    const T* pool = is_v ? (const T*)a.v_pool : (const T*)a.k_pool;
+    const T* fresh = is_v ? (const T*)a.v_new : (const T*)a.k_new;
     const int j0 = kt * kSK;
     for (int e = tid; e < kSK * (D / 4); e += kSThreads) {
       const int jj = e / (D / 4), c = (e % (D / 4)) * 4;
       const int j = j0 + jj;
-      const T* ks = nullptr;
-      const T* vs = nullptr;
+      const T* src = nullptr;
       if (j < kv_hi && j >= cb && j < ce) {
-        const int64_t off = (((int64_t)q0 + (j - cb)) * a.Hkv + kvh) * D + c;
-        ks = (const T*)a.k_new + off;
-        vs = (const T*)a.v_new + off;
+        src = fresh + (((int64_t)q0 + (j - cb)) * a.Hkv + kvh) * D + c;
       } else if (j < kv_hi) {
         int blk = a.block_table[(int64_t)b * a.W + (j >> 4)];
         if (a.check && (blk < 0 || blk >= a.num_blocks)) {
           pkv_raise(a.err, PKV_DEVERR_BLOCK);
           blk = -1;
         }
-        if (blk >= 0) {
-          const int64_t off = (((int64_t)blk * 16 + (j & 15)) * a.Hkv + kvh) * D + c;
-          ks = kpool + off;
-          vs = vpool + off;
-        }
+        if (blk >= 0) src = pool + (((int64_t)blk * 16 + (j & 15)) * a.Hkv + kvh) * D + c;
       }
       if constexpr (sizeof(T) == 4) {
-        cp_async16(kd + jj * LD + c, ks ? (const void*)ks : a.k_pool, ks ? 16 : 0);
-        cp_async16(vd + jj * LD + c, vs ? (const void*)vs : a.v_pool, vs ? 16 : 0);
+        cp_async16(dst + jj * LD + c, src ? (const void*)src : (const void*)pool, src ? 16 : 0);
       } else {
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(kd + jj * LD + c) = ks ? load4<T>(ks) : z;
-        *reinterpret_cast<float4*>(vd + jj * LD + c) = vs ? load4<T>(vs) : z;
+        *reinterpret_cast<float4*>(dst + jj * LD + c) = src ? load4<T>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
-  if (t_begin < t_end) gather(t_begin, 0);
+  // Per tile kt: its values and the next tile's keys are requested at the top (two commit groups), its
+  // keys (requested one tile earlier) are waited for before the scores, its values before P.V.
+  if (t_begin < t_end) gather(t_begin, false, k_buf);
   for (int kt = t_begin; kt < t_end; ++kt) {
     const int j0 = kt * kSK;
-    const int buf = (kt - t_begin) & 1;
-    const float* k_s = kv_buf + buf * 2 * kSK * LD;
-    const float* v_s = k_s + kSK * LD;
-    __syncthreads();  // the previous tile's buffer and P are no longer read
-    if (kt + 1 < t_end) {
-      gather(kt + 1, buf ^ 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's copies have landed
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
+    const float* k_s = k_buf + ((kt - t_begin) & 1) * kSK * LD;
+    __syncthreads();  // the previous tile's P.V no longer reads the values or P
+    gather(kt, true, v_s);
+    if (kt + 1 < t_end)
+      gather(kt + 1, false, k_buf + ((kt + 1 - t_begin) & 1) * kSK * LD);
+    else
+      asm volatile("cp.async.commit_group;" ::: "memory");  // an empty group keeps the count
+    asm volatile("cp.async.wait_group 2;" ::: "memory");  // this tile's keys have landed
     __syncthreads();
 
     // S = Q K^T for rows ty + 16i, keys tx + 16j.
-    float s[4][4];
+    float s[RI][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < RI; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
     {
-      float4 qv[2][4], kv[2][4];
+      float4 qv[2][RI], kv[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[0][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD);
+      for (int i = 0; i < RI; ++i) qv[0][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD);
 #pragma unroll
       for (int j = 0; j < 4; ++j) kv[0][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD);
 #pragma unroll
@@ -280,32 +281,32 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
         const int cur = (d >> 2) & 1, nxt = cur ^ 1;
         if (d + 4 < D) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) qv[nxt][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d + 4);
+          for (int i = 0; i < RI; ++i) qv[nxt][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d + 4);
 #pragma unroll
           for (int j = 0; j < 4; ++j) kv[nxt][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d + 4);
         }
-        // Component by component: 16 independent FMAs between two on the same score.
+        // Component by component: 4 RI independent FMAs between two on the same score.
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < RI; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].x, kv[cur][j].x, s[i][j]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < RI; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].y, kv[cur][j].y, s[i][j]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < RI; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].z, kv[cur][j].z, s[i][j]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < RI; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].w, kv[cur][j].w, s[i][j]);
       }
     }
     // Online softmax per row: the row's 64 scores live in this half-warp (lanes with the same ty).
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RI; ++i) {
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -338,41 +339,54 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
       for (int j = 0; j < 4; ++j) p_s[(tx + 16 * j) * PL + ty + 16 * i] = s[i][j];
       if (tx == 0) alpha_s[ty + 16 * i] = alpha;
     }
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's values have landed
     __syncthreads();
 
-    // O += P V for rows 4ty + i, columns 4tx + 64c.
+    // O += P V for rows RI*ty + i, columns 4tx + 64c.
     {
-      const float4 al = *reinterpret_cast<const float4*>(alpha_s + 4 * ty);
-      const float alr[4] = {al.x, al.y, al.z, al.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int q4 = 0; q4 < RI / 4; ++q4) {
+        const float4 al = *reinterpret_cast<const float4*>(alpha_s + RI * ty + 4 * q4);
+        const float alr[4] = {al.x, al.y, al.z, al.w};
 #pragma unroll
-        for (int c = 0; c < 4 * NC; ++c) acc[i][c] *= alr[i];
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int c = 0; c < 4 * NC; ++c) acc[4 * q4 + e][c] *= alr[e];
+      }
       // Two keys per step: the next key's P and V are loaded while this key's FMAs run.
-      float4 p0 = *reinterpret_cast<const float4*>(p_s + 4 * ty), p1;
-      float4 v0[NC], v1[NC];
+      float4 p0[RI / 4], p1[RI / 4], v0[NC], v1[NC];
+#pragma unroll
+      for (int q4 = 0; q4 < RI / 4; ++q4) p0[q4] = *reinterpret_cast<const float4*>(p_s + RI * ty + 4 * q4);
 #pragma unroll
       for (int c = 0; c < NC; ++c) v0[c] = *reinterpret_cast<const float4*>(v_s + 4 * tx + 64 * c);
-      auto pv_fma = [&](const float4& pv, const float4 (&vv)[NC]) {
-        const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+      auto pv_fma = [&](const float4 (&pv)[RI / 4], const float4 (&vv)[NC]) {
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
+        for (int q4 = 0; q4 < RI / 4; ++q4) {
+          const float pr[4] = {pv[q4].x, pv[q4].y, pv[q4].z, pv[q4].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[i][4 * c + 0] = fmaf(pr[i], vv[c].x, acc[i][4 * c + 0]);
-            acc[i][4 * c + 1] = fmaf(pr[i], vv[c].y, acc[i][4 * c + 1]);
-            acc[i][4 * c + 2] = fmaf(pr[i], vv[c].z, acc[i][4 * c + 2]);
-            acc[i][4 * c + 3] = fmaf(pr[i], vv[c].w, acc[i][4 * c + 3]);
-          }
+          for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float* o = acc[4 * q4 + e] + 4 * c;
+              o[0] = fmaf(pr[e], vv[c].x, o[0]);
+              o[1] = fmaf(pr[e], vv[c].y, o[1]);
+              o[2] = fmaf(pr[e], vv[c].z, o[2]);
+              o[3] = fmaf(pr[e], vv[c].w, o[3]);
+            }
+        }
       };
 #pragma unroll 4
       for (int k = 0; k < kSK; k += 2) {
-        p1 = *reinterpret_cast<const float4*>(p_s + (k + 1) * PL + 4 * ty);
+#pragma unroll
+        for (int q4 = 0; q4 < RI / 4; ++q4)
+          p1[q4] = *reinterpret_cast<const float4*>(p_s + (k + 1) * PL + RI * ty + 4 * q4);
 #pragma unroll
         for (int c = 0; c < NC; ++c) v1[c] = *reinterpret_cast<const float4*>(v_s + (k + 1) * LD + 4 * tx + 64 * c);
         pv_fma(p0, v0);
         if (k + 2 < kSK) {
-          p0 = *reinterpret_cast<const float4*>(p_s + (k + 2) * PL + 4 * ty);
+#pragma unroll
+          for (int q4 = 0; q4 < RI / 4; ++q4)
+            p0[q4] = *reinterpret_cast<const float4*>(p_s + (k + 2) * PL + RI * ty + 4 * q4);
 #pragma unroll
           for (int c = 0; c < NC; ++c) v0[c] = *reinterpret_cast<const float4*>(v_s + (k + 2) * LD + 4 * tx + 64 * c);
         }
@@ -380,20 +394,21 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
       }
     }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing in flight into shared memory at exit
 
   // Epilogue: each row's softmax state to shared memory, then the normalised output (one split),
   // or the partial output and its natural-log log-sum-exp (a key-range split).
   if (tx == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RI; ++i) {
       l_s[ty + 16 * i] = l[i];
       m_s[ty + 16 * i] = m[i];
     }
   }
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 4 * ty + i;
+  for (int i = 0; i < RI; ++i) {
+    const int r = RI * ty + i;
     const int qi = i0 + r;
     if (qi >= Sq) continue;
     const int64_t tok = (int64_t)q0 + qi;

@@ -201,7 +201,7 @@ SplitPlan plan_splits(int64_t items, int64_t tiles, int sms, int max_splits) {
 }  // namespace
 
 // Key-range splits the call plans from host-visible sizes.  An item is what one CTA of the
-// unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 64 for the
+// unsplit launch covers: 256 queries of one (row, head) for the tensor-core kernel, 128 for the
 // CUDA-core one.  Both kernels split only the tail behind whole waves (every item when there
 // are fewer items than CTA slots).  The CUDA-core kernel's tail runs as a one-dimensional grid,
 // whose size must stay a valid grid dimension.

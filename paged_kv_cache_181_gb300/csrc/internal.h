@@ -21,8 +21,8 @@ inline int pkv_dtype_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
 constexpr int kPkvMaxSplits = 16;
 
 // CUDA-core attention kernel: queries per CTA, keys per tile, CTAs resident per SM (its shared memory
-// holds the fp32 Q, K, V and P tiles: one CTA per SM for D = 128).  The split planner counts in these.
-constexpr int kSimtItemRows = 64;
+// holds the fp32 Q, K, V and P tiles: one CTA per SM).  The split planner counts in these.
+constexpr int kSimtItemRows = 128;
 constexpr int kSimtKeyTile = 64;
 constexpr int kSimtCtasPerSm = 1;
 
@@ -56,7 +56,7 @@ struct PkvAttnArgs {
   // the combine.  0: every item is split.
   int split_direct;
   // Which kernel's items the split tail counts: 0 the tensor-core kernel's (256 queries of one
-  // row and head, pkv_tc_item order), 1 the CUDA-core kernel's (64 queries; the row's query
+  // row and head, pkv_tc_item order), 1 the CUDA-core kernel's (128 queries; the row's query
   // tiles fastest, then the rows, then the heads).
   int simt_items;
   int check;

@@ -105,6 +105,9 @@ def compare(got: np.ndarray, want: np.ndarray, dtype: str, mask=None) -> tuple[f
 
 TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 2e-3), "f16": (2e-2, 2e-3)}
 
+# Queries per CTA of the CUDA-core kernel: the unit its split planner counts items in.
+SIMT_ITEM_ROWS = 128
+
 
 # Small workloads covering edge cases: D=64, GQA 3, ragged tails, fp16, a single query, a single key,
 # causal-only masks, batch 1 with an exact 256-query tile boundary.

@@ -26,6 +26,10 @@ VARIANTS = [
     dataclasses.replace(SMALL, name="packed-small-f16-d64", dtype="f16", head_dim=64, num_heads=4, num_kv_heads=4,
                         seed=33),
     dataclasses.replace(SMALL, name="packed-small-f32", dtype="f32", head_dim=64, seed=34),
+    # 12 heads: the CUDA-core kernel's items (128 queries) are 6 rows x 12 heads x 3 = 216, one wave of 152
+    # SMs and a tail of 64 that splits, rows of every length among them.
+    dataclasses.replace(SMALL, name="packed-small-f32-h12", dtype="f32", head_dim=64, num_heads=12,
+                        num_kv_heads=4, seed=35),
 ]
 
 
@@ -46,10 +50,9 @@ def test_packed_rows_parity(pb, splits):
 
     pc, out = _run(pb, flags=_lib.PKV_SPLITS(splits) if splits else 0)
     if pb.dtype == "f32" and not splits:
-        # The CUDA-core kernel's items (64 queries): 6 rows x 6 heads x 5 = 180, one wave of 152 SMs and a
-        # tail of 28 that splits, rows of every length among them.
+        # With more items than SMs, the CUDA-core kernel runs its whole waves whole and splits the tail.
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        items = len(pb.rows) * pb.num_heads * -(-max(r.query_len for r in pb.rows) // 64)
+        items = len(pb.rows) * pb.num_heads * -(-max(r.query_len for r in pb.rows) // cases.SIMT_ITEM_ROWS)
         got_splits, whole = _lib.last_split_plan()
         if items > sms and items % sms:
             assert got_splits > 1 and whole == items // sms * sms, (got_splits, whole)

@@ -206,15 +206,15 @@ def test_split_tail_shrinks_to_the_workspace(lib):
 
 
 def _simt_whole_items(w, sms):
-    """Items the CUDA-core kernel runs whole: its whole waves of 64-query items (one CTA per SM)."""
-    items = w.batch * w.num_heads * -(-w.q_len // 64)
+    """Items the CUDA-core kernel runs whole: its whole waves of items (one CTA per SM)."""
+    items = w.batch * w.num_heads * -(-w.q_len // cases.SIMT_ITEM_ROWS)
     return items // sms * sms, items
 
 
 def test_negative_scale_plans_for_the_kernel_that_runs(lib):
     """A negative softmax scale on bf16 is refused unless the CUDA-core kernel is asked for by name; then it
-    runs there, with that kernel's split plan (its own 64-query items: 4 whole waves and a split tail of
-    32), and matches the oracle."""
+    runs there, with that kernel's split plan (its own items of 128 queries: two whole waves and a split
+    tail of 16), and matches the oracle."""
     from paged_kv_cache_181_gb300 import workload
 
     w = _tail_workload()
@@ -232,8 +232,8 @@ def test_negative_scale_plans_for_the_kernel_that_runs(lib):
 
 @pytest.mark.parametrize("fused", [False, True], ids=["two-call", "fused"])
 def test_cuda_core_split_tail_long_window_f32(lib, fused):
-    """fp32 at the long window's full size: 2000 CUDA-core items of 64 queries are 13 waves of 152 SMs and
-    24 more; those 24 split their 415 key tiles and the combine merges them, the rest run whole.  Sampled
+    """fp32 at the long window's full size: 1040 CUDA-core items of 128 queries are 6 waves of 152 SMs and
+    128 more; those 128 split their 415 key tiles and the combine merges them, the rest run whole.  Sampled
     rows of every (row, head) -- the tail's included -- against the float64 oracle."""
     from paged_kv_cache_181_gb300 import workload
 

@@ -1,9 +1,10 @@
 """Host: the key-range split the library plans, read through paged_attn_workspace_size (no GPU needed).
 
-The workspace a call may use is max(8, planned splits) x Tq x Hq x (D + 1) x 4 bytes, so the planned split
-count of the tensor-core kernel shows in it.  Without a device the planner assumes GB300's 152 SMs.  The
-expected counts are the ones the GPU sweeps measured best for these workloads (and the rule's boundaries):
-whole waves of 256-query items run unsplit and only a last, partly filled wave is split.
+The workspace a call may use is max(8, planned splits) x Tq x Hq x (D + 1) x 4 bytes, the planned splits
+being the larger of the two kernels' plans (256-query items for the tensor-core kernel, 128-query items for
+the CUDA-core one), so the planned split count shows in it.  Without a device the planner assumes GB300's 152
+SMs.  The expected counts are the ones the GPU sweeps measured best for these workloads (and the rule's
+boundaries): whole waves of items run unsplit and only a last, partly filled wave is split.
 """
 
 import pytest
@@ -31,8 +32,9 @@ def _no_device():
     ("mixed mask", (8192, 24, 128, 2, 4096, 8208), 13),
     # 8 items, fewer than the SMs: every item splits 16 ways
     ("few heads", (256, 8, 128, 1, 256, 26528), 16),
-    # 168 items = 1 wave + 16: the tail splits 9 ways
-    ("one frame", (3120, 12, 128, 2, 1560, 6272), 9),
+    # 168 items = 1 wave + 16: the tail splits 9 ways; the CUDA-core kernel's 312 items = 2 waves + 8, whose
+    # tail splits 14 ways, set the workspace
+    ("one frame", (3120, 12, 128, 2, 1560, 6272), 14),
 ])
 def test_planned_splits_of_the_workloads(name, sizes, splits):
     assert planned(*sizes) == splits

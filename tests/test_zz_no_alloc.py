@@ -17,6 +17,8 @@ import torch
 
 from oracle import pagedattn as pa
 
+from . import cases
+
 pytestmark = pytest.mark.gpu
 
 TOL = {torch.float32: (1e-4, 1e-4), torch.bfloat16: (2e-2, 2e-3), torch.float16: (2e-2, 2e-3)}
@@ -123,12 +125,12 @@ def test_noalloc_planned_splits(lib):
 
 
 def test_noalloc_cuda_core_split_tail(lib):
-    # fp32 runs on the CUDA-core kernel, whose items are 64 queries: 8 heads x 1280 queries = 160 items, one
+    # fp32 runs on the CUDA-core kernel, whose items are 128 queries: 16 heads x 1280 queries = 160 items, one
     # wave of 152 SMs and a tail of 8 that splits into the scratch while the rest run whole.
-    c = make_case(8, torch.float32, 8, 8, 64, (1280,), (3000,), ([(1720, 3000)],))
+    c = make_case(8, torch.float32, 16, 4, 64, (1280,), (1400,), ([(120, 1400)],))
     ref, got, launches, ref_plan, plan = run_both(lib, c, 0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    items = 8 * 1280 // 64
+    items = 16 * 1280 // cases.SIMT_ITEM_ROWS
     if items > sms and items % sms:
         assert plan[0] > 1 and plan[1] == items // sms * sms and launches == 2, (plan, launches)
     assert plan == ref_plan, (plan, ref_plan)
