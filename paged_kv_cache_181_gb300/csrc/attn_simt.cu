@@ -40,22 +40,22 @@
 
 namespace {
 
-constexpr int kSQ = kSimtItemRows;  // queries per CTA
+constexpr int kSQ = kSimtItemRows;  // queries per item (the unit of the grid and the split planner)
 constexpr int kSK = kSimtKeyTile;   // keys per tile
 constexpr int kSThreads = 256;
 constexpr int kSWarps = kSThreads / 32;
 
-constexpr int RI = kSQ / 16;        // query rows per thread (scores: ty + 16i; output: RI*ty + i)
-static_assert(kSQ % 64 == 0 && kSK == 64, "thread tiles assume 64-key tiles and 64k-query CTAs");
+static_assert(kSQ == 128 && kSK == 64, "thread tiles assume 128-query items and 64-key tiles");
 
-template <int D>
+// Shared memory of a CTA over ROWS query rows (128; 64 when every row of the call has at most 64 queries).
+template <int D, int ROWS>
 struct SimtSmem {
-  static constexpr int LD = D + 4;    // row stride (floats) of Q, K and V: 16-byte rows, staggered banks
-  static constexpr int PL = kSQ + 4;  // row stride of P^T
+  static constexpr int LD = D + 4;     // row stride (floats) of Q, K and V: 16-byte rows, staggered banks
+  static constexpr int PL = ROWS + 4;  // row stride of P^T
   // Q, two key buffers (the next tile's keys load while this one is used), one value buffer (a tile's
   // values load during its scores and softmax), P^T, per-row state.
-  static constexpr size_t floats = (size_t)kSQ * LD + (size_t)3 * kSK * LD + (size_t)kSK * PL + 3 * kSQ;
-  static constexpr size_t bytes = floats * sizeof(float) + (kSQ + 1) * sizeof(int);
+  static constexpr size_t floats = (size_t)ROWS * LD + (size_t)3 * kSK * LD + (size_t)kSK * PL + 3 * ROWS;
+  static constexpr size_t bytes = floats * sizeof(float) + (ROWS + 1) * sizeof(int);
 };
 
 // 16-byte asynchronous copy global -> shared; `bytes` 0 zero-fills the destination without a read.
@@ -90,20 +90,23 @@ PKV_DEVINLINE void store4(T* p, float x0, float x1, float x2, float x3) {
   }
 }
 
-template <typename T, int D>
+// RI query rows per thread (scores: rows ty + 16i; output: rows RI*ty + i): 8 for a whole 128-query item,
+// 4 when every row of the call has at most 64 queries (the CTA then covers its item's first 64 rows only).
+template <typename T, int D, int RI>
 __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) {
-  using SM = SimtSmem<D>;
+  constexpr int ROWS = 16 * RI;
+  using SM = SimtSmem<D, ROWS>;
   constexpr int LD = SM::LD, PL = SM::PL, NC = D / 64;
   extern __shared__ __align__(16) float sm[];
-  float* q_s = sm;                          // [kSQ][LD]
-  float* k_buf = q_s + kSQ * LD;            // two buffers of [kSK][LD] keys
+  float* q_s = sm;                          // [ROWS][LD]
+  float* k_buf = q_s + ROWS * LD;           // two buffers of [kSK][LD] keys
   float* v_s = k_buf + 2 * kSK * LD;        // [kSK][LD] values
   float* p_s = v_s + kSK * LD;              // [kSK][PL], P transposed: p_s[key * PL + query]
-  float* alpha_s = p_s + kSK * PL;  // [kSQ] per-tile rescale of each row's O
-  float* l_s = alpha_s + kSQ;       // [kSQ]
-  float* m_s = l_s + kSQ;           // [kSQ]
-  int* lim_s = reinterpret_cast<int*>(m_s + kSQ);  // [kSQ], then the CTA's largest limit
-  int* kv_hi_s = lim_s + kSQ;
+  float* alpha_s = p_s + kSK * PL;  // [ROWS] per-tile rescale of each row's O
+  float* l_s = alpha_s + ROWS;      // [ROWS]
+  float* m_s = l_s + ROWS;          // [ROWS]
+  int* lim_s = reinterpret_cast<int*>(m_s + ROWS);  // [ROWS], then the CTA's largest limit
+  int* kv_hi_s = lim_s + ROWS;
 
   // CTA -> (row, query tile, head, key-range split).  Without a split tail the grid is (rows x
   // query tiles, heads, splits).  With one it is one-dimensional over the items in the same order
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
   }
   const int base = pkv_query_base(L, Sq, a.segs, s_begin, s_end);
   // Per-query key limits from the row's segments.
-  if (tid < kSQ) {
+  if (tid < ROWS) {
     const int i = i0 + tid;
     int lim = 0;
     if (i < Sq) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
     lim_s[tid] = lim;
   }
   // Query tile, fp32 in shared memory (rows past the row's queries are zero).
-  for (int e = tid; e < kSQ * (D / 4); e += kSThreads) {
+  for (int e = tid; e < ROWS * (D / 4); e += kSThreads) {
     const int r = e / (D / 4), c = (e % (D / 4)) * 4;
     const int i = i0 + r;
     const float4 x = i < Sq ? load4<T>((const T*)a.q + ((int64_t)(q0 + i) * a.Hq + h) * D + c)
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
   if (warp == 0) {
     int hi = 0;
 #pragma unroll
-    for (int r = lane; r < kSQ; r += 32) hi = lim_s[r] > hi ? lim_s[r] : hi;
+    for (int r = lane; r < ROWS; r += 32) hi = lim_s[r] > hi ? lim_s[r] : hi;
     hi = __reduce_max_sync(0xffffffffu, hi);
     if (lane == 0) *kv_hi_s = hi;
   }
@@ -562,9 +565,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(PkvAttnArgs a) {
     combine_row<T, 2, kBatch>(a, item, lane);
 }
 
-template <typename T, int D>
-int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
-  const size_t smem = SimtSmem<D>::bytes;
+template <typename T, int D, int RI>
+int launch_simt_r(const PkvAttnArgs& a, cudaStream_t s) {
+  const size_t smem = SimtSmem<D, 16 * RI>::bytes;
   // Keyed on the context: function attributes belong to the context they were set in.
   static std::atomic<uint64_t> attr_set[64];
   int dev = 0;
@@ -573,7 +576,7 @@ int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
   const uint64_t ctx = pkv_context_id();
   if (!cached || ctx == 0 || attr_set[dev].load(std::memory_order_acquire) != ctx) {
     const cudaError_t e =
-        cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(attn_simt_kernel<T, D, RI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     if (cached) attr_set[dev].store(ctx, std::memory_order_release);
   }
@@ -585,8 +588,15 @@ int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
     if (ctas > 0x7fffffff) return (int)cudaErrorInvalidConfiguration;  // the planner keeps it below
     grid = dim3((unsigned)ctas);
   }
-  attn_simt_kernel<T, D><<<grid, kSThreads, smem, s>>>(a);
+  attn_simt_kernel<T, D, RI><<<grid, kSThreads, smem, s>>>(a);
   return (int)cudaGetLastError();
+}
+
+// Rows of at most 64 queries (every item then holds only those): the CTA covers 64 rows with 4 per thread,
+// half the work of a 128-row CTA whose other rows would be padding.  The items are the same either way.
+template <typename T, int D>
+int launch_simt_d(const PkvAttnArgs& a, cudaStream_t s) {
+  return a.max_query_len <= 64 ? launch_simt_r<T, D, 4>(a, s) : launch_simt_r<T, D, 8>(a, s);
 }
 
 template <typename T>
