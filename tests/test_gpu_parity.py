@@ -125,7 +125,7 @@ MEDIUM = [
                         seed=41),
     # fp16 end to end on the one-frame geometry
     dataclasses.replace(configs.ONE_FRAME, name="one-frame-f16", dtype="f16", seed=42),
-    # fp32 at full size: the CUDA-core kernel's 64-key tiles (98 per row) through its double-buffered copies
+    # fp32 at full size: the CUDA-core kernel's 64-key tiles (98 per row) through its asynchronous copies
     dataclasses.replace(configs.ONE_FRAME, name="one-frame-f32", dtype="f32", seed=43),
 ]
 
