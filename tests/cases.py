@@ -130,6 +130,11 @@ EDGE = [
     dataclasses.replace(configs.ONE_FRAME, name="edge-b1-256", batch=1, num_heads=2, num_kv_heads=1,
                         chunk_tokens=256, window_chunks=3, sink_chunks=0, history_tokens=512, query_tokens=256,
                         pool_blocks=128, seed=25),
+    # fp32 at the CUDA-core kernel's row boundary: 64 queries per row run its 64-row CTAs, 65 its 128-row ones
+    dataclasses.replace(configs.TINY, name="edge-f32-q64", chunk_tokens=64, window_chunks=2, history_tokens=64,
+                        query_tokens=64, seed=26),
+    dataclasses.replace(configs.TINY, name="edge-f32-q65", chunk_tokens=65, window_chunks=2, history_tokens=65,
+                        query_tokens=65, seed=27),
 ]
 
 
