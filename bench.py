@@ -940,8 +940,11 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
         up.wait_event(start)  # no upload of the timed steps starts before the clock does
         # Steps are pipelined: a step's last read-backs overlap the next step's first layers (its output
         # buffers are the other set's); the last step ends with every read-back done.
+        marks = [start]
         for i in range(steps):
             e2e_step(last=i == steps - 1)
+            marks.append(torch.cuda.Event(enable_timing=True))
+            marks[-1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -957,6 +960,7 @@ def run_e2e(case, args, world, stream, fused: bool, gpu_index: int = 0):
             "d2h_bytes_per_step": d2h, "steps": steps, "api": f"{api} per layer, inputs from pinned host memory",
             "upload_ms_alone": upload_ms, "h2d_gbs_alone": h2d / (upload_ms * 1e-3) / 1e9,
             "h2d_gbs_alone_after": h2d / (upload_ms_after * 1e-3) / 1e9,
+            "step_ms": [round(marks[i].elapsed_time(marks[i + 1]), 3) for i in range(steps)],
             "upload_ms_in_last_step": sum(up_t[l][0].elapsed_time(up_t[l][1]) for l in range(layers)),
             "compute_ms_in_last_step": sum(cp_t[l][0].elapsed_time(cp_t[l][1]) for l in range(layers)),
             "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
