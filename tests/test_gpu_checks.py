@@ -78,8 +78,10 @@ def test_bad_slot_is_flagged_and_skipped(lib):
 def test_empty_row_and_ragged_batch_match_oracle(lib):
     from oracle import pagedattn as pa
 
-    for dtype, flags in ((torch.bfloat16, 0), (torch.float32, 0), (torch.bfloat16, lib.PKV_FORCE_SIMT)):
-        q, kp, vp, table, qsl, seq = small_inputs(dtype=dtype, B=3, sq=(20, 0, 3), L=(40, 5, 17), W=4)
+    # D 64 and 128; every row of at most 64 queries, so the CUDA-core kernel runs its 64-row CTAs.
+    for d, dtype, flags in ((64, torch.bfloat16, 0), (64, torch.float32, 0), (64, torch.bfloat16, lib.PKV_FORCE_SIMT),
+                            (128, torch.float32, 0), (128, torch.bfloat16, lib.PKV_FORCE_SIMT)):
+        q, kp, vp, table, qsl, seq = small_inputs(dtype=dtype, d=d, B=3, sq=(20, 0, 3), L=(40, 5, 17), W=4)
         out = lib.paged_attn_varlen(q, kp, vp, table, qsl, seq, 20, 64, 0.3, flags=flags)
         torch.cuda.synchronize()
         want = pa.paged_attention(q.float().cpu().numpy(), kp.float().cpu().numpy(), vp.float().cpu().numpy(),
