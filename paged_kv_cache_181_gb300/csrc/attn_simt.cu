@@ -14,9 +14,9 @@
 //              (j < 4): per 4 dimensions it loads 8 query and 4 key float4s and
 //              does 128 FMAs (rows and keys interleaved by 16, so a warp's key
 //              loads hit distinct banks and its query loads are broadcasts);
-//              the next 4 dimensions' operands are loaded while these FMAs run
-//              (two warps per SM partition cannot hide shared-memory latency
-//              otherwise);
+//              the loop is unrolled, so the next dimensions' operands load while
+//              these FMAs run (two warps per SM partition cannot hide shared-
+//              memory latency otherwise);
 //   softmax    each row's 64 scores sit in the 16 threads of one half-warp:
 //              maxima and sums by shuffles; P goes to shared memory transposed;
 //   O += P V   thread (ty, tx) owns rows 8ty..8ty+7 and columns 4tx + 64c:
@@ -274,37 +274,29 @@ __global__ void __launch_bounds__(kSThreads, 1) attn_simt_kernel(PkvAttnArgs a) 
 #pragma unroll
       for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
     {
-      float4 qv[2][RI], kv[2][4];
-#pragma unroll
-      for (int i = 0; i < RI; ++i) qv[0][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) kv[0][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD);
 #pragma unroll
       for (int d = 0; d < D; d += 4) {
-        const int cur = (d >> 2) & 1, nxt = cur ^ 1;
-        if (d + 4 < D) {
+        float4 qv[RI], kv[4];
 #pragma unroll
-          for (int i = 0; i < RI; ++i) qv[nxt][i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d + 4);
+        for (int i = 0; i < RI; ++i) qv[i] = *reinterpret_cast<const float4*>(q_s + (ty + 16 * i) * LD + d);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) kv[nxt][j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d + 4);
-        }
-        // Component by component: 4 RI independent FMAs between two on the same score.
+        for (int j = 0; j < 4; ++j) kv[j] = *reinterpret_cast<const float4*>(k_s + (tx + 16 * j) * LD + d);
 #pragma unroll
         for (int i = 0; i < RI; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].x, kv[cur][j].x, s[i][j]);
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[i].x, kv[j].x, s[i][j]);
 #pragma unroll
         for (int i = 0; i < RI; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].y, kv[cur][j].y, s[i][j]);
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[i].y, kv[j].y, s[i][j]);
 #pragma unroll
         for (int i = 0; i < RI; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].z, kv[cur][j].z, s[i][j]);
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[i].z, kv[j].z, s[i][j]);
 #pragma unroll
         for (int i = 0; i < RI; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[cur][i].w, kv[cur][j].w, s[i][j]);
+          for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[i].w, kv[j].w, s[i][j]);
       }
     }
     // Online softmax per row: the row's 64 scores live in this half-warp (lanes with the same ty).
