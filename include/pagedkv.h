@@ -287,7 +287,7 @@ PKV_API size_t paged_attn_workspace_size(int64_t Tq, int Hq, int D, int B, int m
  *   softmax_scale    multiplies Q.K (the pages pass D^-0.5).  For bf16/f16 it must be > 0: the
  *                    tensor-core kernel requires it, and any other value returns PKV_ERR_UNSUPPORTED
  *                    unless flags holds PKV_FORCE_SIMT, which runs the CUDA-core kernel (any finite
- *                    scale, about two orders of magnitude slower).  fp32 takes any finite scale.
+ *                    scale, about 50 times slower on bf16).  fp32 takes any finite scale.
  * A query that sees no key (only possible with ill-formed segments) gets 0.
  * Tq == 0, B == 0 or max_query_len == 0: nothing to compute; PKV_OK without a launch
  * (sizes and the dtype are still validated; out is not touched).

@@ -254,7 +254,7 @@ pkv_status attn_impl(const char* fn, const void* q, int64_t Tq, int Hq, const vo
     return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dt);
   if (!isfinite(softmax_scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "%s: softmax_scale is not finite", fn);
   // The tensor-core kernel keeps its running maximum for a positive scale only; the CUDA-core kernel,
-  // two orders of magnitude slower, takes any scale, but only when asked for by name.
+  // about 50 times slower on bf16, takes any scale, but only when asked for by name.
   if (dt != PKV_F32 && !(softmax_scale > 0.f) && !(flags & PKV_FORCE_SIMT))
     return pkv_fail(PKV_ERR_UNSUPPORTED,
                     "%s: a bf16/f16 call needs softmax_scale > 0 (got %g); pass PKV_FORCE_SIMT to run it on the "
