@@ -56,6 +56,10 @@ def _run(cmd: list[str], verbose: bool, log: str | None = None) -> str:
 # bf16/f16 call at run time (the launcher keeps the same check as a backstop).
 TC_SOURCE = "attn_tc.cu"
 TC_KERNEL = "attn_tc_kernel"
+# Sources whose ptxas report is kept beside their object (`<source>.ptxas.txt`): the tensor-core kernel's for
+# the gate below, the CUDA-core kernel's for its spill check (it runs at 252-254 registers, where a
+# toolchain that allocated differently would start spilling: slower, not wrong).
+PTXAS_LOGGED = (TC_SOURCE, "attn_simt.cu")
 
 
 def expected_tc_registers(source: str) -> int:
@@ -90,6 +94,23 @@ def check_tc_registers(ptxas_log: str, expected: int) -> int:
     return seen
 
 
+def spills(ptxas_log: str, kernel: str) -> list[tuple[str, int, int]]:
+    """(function, spill store bytes, spill load bytes) of every instantiation of ``kernel`` in a
+    ``-Xptxas -v`` log."""
+    out = []
+    current = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"(?:Compiling entry function|Function properties for) '?([^' ]+)'?", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m and current is not None and kernel in current:
+            out.append((current, int(m.group(1)), int(m.group(2))))
+            current = None
+    return out
+
+
 def _stale(obj: str, deps: list[str]) -> bool:
     if not os.path.exists(obj):
         return True
@@ -110,13 +131,13 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         path = os.path.join(CSRC, src)
         obj = os.path.join(OUT_DIR, src + ".o")
         objs.append(obj)
-        is_tc = src == TC_SOURCE
-        if force or _stale(obj, [path, *headers]) or (is_tc and _stale(tc_log, [obj])):
+        log = os.path.join(OUT_DIR, src + ".ptxas.txt") if src in PTXAS_LOGGED else None
+        if force or _stale(obj, [path, *headers]) or (log is not None and _stale(log, [obj])):
             cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                    "-I", INCLUDE, "-I", CSRC, "-c", path, "-o", obj]
-            if ptxas_verbose or is_tc:
+            if ptxas_verbose or log is not None:
                 cmd += ["-Xptxas", "-v"]
-            jobs.append((cmd, tc_log if is_tc else None))
+            jobs.append((cmd, log))
     for src in HOST_SOURCES:
         path = os.path.join(CSRC, src)
         obj = os.path.join(OUT_DIR, src + ".o")

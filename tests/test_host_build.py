@@ -1,4 +1,5 @@
-"""CPU: the build's register-count gate and the host-side refusal of a non-positive bf16/f16 scale."""
+"""CPU: the build's register-count gate, the CUDA-core kernel's spill check, and the host-side refusal of a
+non-positive bf16/f16 scale."""
 
 import os
 
@@ -41,6 +42,37 @@ def test_register_gate_reads_the_sized_count_from_the_source():
     if os.path.exists(log):
         with open(log) as f:
             assert b.check_tc_registers(f.read(), n) == 4  # D in {64, 128} x {bf16, f16}
+
+
+SPILL_LOG = """ptxas info    : Compiling entry function '_ZN3foo16attn_simt_kernelIfLi128ELi8EEEv' for 'sm_103a'
+ptxas info    : Function properties for _ZN3foo16attn_simt_kernelIfLi128ELi8EEEv
+    0 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads
+ptxas info    : Used 252 registers, used 1 barriers
+ptxas info    : Compiling entry function '_ZN3foo12other_kernelEv' for 'sm_103a'
+ptxas info    : Function properties for _ZN3foo12other_kernelEv
+    8 bytes stack frame, 8 bytes spill stores, 8 bytes spill loads
+ptxas info    : Compiling entry function '_ZN3foo16attn_simt_kernelIfLi64ELi4EEEv' for 'sm_103a'
+ptxas info    : Function properties for _ZN3foo16attn_simt_kernelIfLi64ELi4EEEv
+    16 bytes stack frame, 12 bytes spill stores, 20 bytes spill loads
+ptxas info    : Used 255 registers, used 1 barriers
+"""
+
+
+def test_spill_report_is_read_per_instantiation():
+    got = b.spills(SPILL_LOG, "attn_simt_kernel")
+    assert got == [("_ZN3foo16attn_simt_kernelIfLi128ELi8EEEv", 0, 0), ("_ZN3foo16attn_simt_kernelIfLi64ELi4EEEv", 12, 20)]
+
+
+def test_cuda_core_kernel_does_not_spill():
+    # The library built in this tree: every instantiation (fp32/bf16/f16 x D 64/128 x 4/8 rows per thread)
+    # fits its registers.
+    log = os.path.join(b.OUT_DIR, "attn_simt.cu.ptxas.txt")
+    if not os.path.exists(log):
+        pytest.skip("no ptxas report of the CUDA-core kernel in this tree")
+    with open(log) as f:
+        got = b.spills(f.read(), "attn_simt_kernel")
+    assert len(got) == 12
+    assert all(st == 0 and ld == 0 for _, st, ld in got), got
 
 
 def test_non_positive_scale_is_refused_for_16_bit_inputs():
